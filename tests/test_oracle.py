@@ -1,0 +1,271 @@
+"""Pins for the fp64 oracle: it is checked against things other than itself.
+
+Each test ties one part of the oracle to a fact fixed by the pages or by
+mathematics, chosen so a plausible slip (wrong fp16 decode, dropped
+normalisation, wrong query-head -> KV-head map, wrong table index, reading
+past the row's length, wrong merge weight) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import brute
+from paged_kv_cache_06_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _f16(a):
+    return np.asarray(a, dtype=np.float16).view(np.uint16)
+
+
+def _rand_case(seed, lengths, bs, hq=4, hk=2, d=8, extra=3, nan=True):
+    return wl.custom(lengths, bs, seed=seed, append=False, nan_fill=nan, extra_blocks=extra,
+                     q_heads=hq, kv_heads=hk, head_dim=d)
+
+
+# --- fp16 decoding -----------------------------------------------------------
+
+def test_half_decode_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ours = oracle.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zero is kept
+    assert math.copysign(1.0, ours[0x8000]) == -1.0
+
+
+# --- brute force ---------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,lengths,bs", [
+    (1, [1, 2, 3], 1), (2, [5, 0, 7], 2), (3, [4, 9], 3), (4, [8, 8, 1, 13], 4), (5, [6], 5)])
+def test_oracle_matches_pure_python_brute_force(seed, lengths, bs):
+    c = _rand_case(seed, lengths, bs)
+    ours = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    ref = np.array(brute.paged_decode(c.q[0].tolist(), c.k_pool[0].tolist(), c.v_pool[0].tolist(),
+                                      c.block_tables.tolist(), c.seq_lens.tolist(), c.scale))
+    ref = ref.reshape(ours.shape)
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_golden_hand_worked_decode():
+    g = json.load(open(os.path.join(GOLDEN, "decode_hand.json")))
+    out = oracle.paged_decode(_f16(g["q"]), _f16(g["k_pool"]), _f16(g["v_pool"]),
+                              np.array(g["block_tables"], np.int32),
+                              np.array(g["seq_lens"], np.int32), g["scale"])
+    np.testing.assert_allclose(out, np.array(g["expected"]), rtol=1e-14, atol=1e-14)
+
+
+# --- closed forms and special cases --------------------------------------------
+
+def test_one_token_row_returns_v_exactly():
+    c = _rand_case(7, [1, 1, 1], 4)
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    group = c.q_heads // c.kv_heads
+    for r in range(c.rows):
+        pb = c.block_tables[r, 0]
+        for h in range(c.q_heads):
+            v = oracle.half_to_double(c.v_pool[0, pb, 0, h // group])
+            assert np.array_equal(out[r, h], v)
+
+
+def test_constant_v_returns_that_v():
+    c = _rand_case(8, [9, 30], 4, nan=False)
+    v = c.v_pool.copy()
+    const = _f16(np.linspace(-2, 2, c.head_dim))
+    v[...] = const  # every token of every head carries the same V
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], v[0], c.block_tables, c.seq_lens, c.scale)
+    np.testing.assert_allclose(out, np.broadcast_to(oracle.half_to_double(const), out.shape),
+                               rtol=1e-14, atol=1e-15)
+
+
+def test_equal_keys_give_the_plain_mean_of_v():
+    c = _rand_case(9, [11, 4], 3, nan=False)
+    k = c.k_pool.copy()
+    k[...] = _f16(np.full(c.head_dim, 0.75))
+    out = oracle.paged_decode(c.q[0], k[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    group = c.q_heads // c.kv_heads
+    for r in range(c.rows):
+        toks = [(c.block_tables[r, t // 3], t % 3) for t in range(c.seq_lens[r])]
+        for h in range(c.q_heads):
+            vs = np.stack([oracle.half_to_double(c.v_pool[0, pb, s, h // group]) for pb, s in toks])
+            np.testing.assert_allclose(out[r, h], np.mean(vs, axis=0), rtol=1e-13, atol=1e-14)
+
+
+def test_zero_scale_gives_the_plain_mean_of_v():
+    c = _rand_case(10, [7], 2, nan=False)
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, 0.0)
+    group = c.q_heads // c.kv_heads
+    toks = [(c.block_tables[0, t // 2], t % 2) for t in range(7)]
+    for h in range(c.q_heads):
+        vs = np.stack([oracle.half_to_double(c.v_pool[0, pb, s, h // group]) for pb, s in toks])
+        np.testing.assert_allclose(out[0, h], vs.mean(axis=0), rtol=1e-13, atol=1e-14)
+
+
+def test_two_tokens_follow_the_logistic_closed_form():
+    # softmax of two scores is (1 - sigma(s1 - s0), sigma(s1 - s0))
+    c = _rand_case(11, [2], 1, nan=False)
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    group = c.q_heads // c.kv_heads
+    b0, b1 = c.block_tables[0, 0], c.block_tables[0, 1]
+    for h in range(c.q_heads):
+        kvh = h // group
+        qv = oracle.half_to_double(c.q[0, 0, h])
+        k0 = oracle.half_to_double(c.k_pool[0, b0, 0, kvh])
+        k1 = oracle.half_to_double(c.k_pool[0, b1, 0, kvh])
+        v0 = oracle.half_to_double(c.v_pool[0, b0, 0, kvh])
+        v1 = oracle.half_to_double(c.v_pool[0, b1, 0, kvh])
+        w1 = scipy.special.expit(c.scale * (np.dot(qv, k1) - np.dot(qv, k0)))
+        np.testing.assert_allclose(out[0, h], v0 + w1 * (v1 - v0), rtol=1e-12, atol=1e-13)
+
+
+def test_dominant_score_selects_its_token_without_overflow():
+    # a huge score must not overflow: the result is that token's V
+    c = _rand_case(12, [5], 5, hq=2, hk=1, d=8, nan=False)
+    q = c.q.copy(); k = c.k_pool.copy()
+    q[...] = _f16(np.full(8, 8.0))
+    k[0, c.block_tables[0, 0]] = _f16(np.zeros(8))
+    k[0, c.block_tables[0, 0], 3] = _f16(np.full(8, 60000.0))
+    out = oracle.paged_decode(q[0], k[0], c.v_pool[0], c.block_tables, c.seq_lens, 1.0)
+    v = oracle.half_to_double(c.v_pool[0, c.block_tables[0, 0], 3, 0])
+    assert np.all(np.isfinite(out))
+    np.testing.assert_allclose(out[0, 0], v, rtol=0, atol=1e-300)
+
+
+def test_gqa_maps_contiguous_query_head_groups_to_kv_heads():
+    # Hq=6, Hk=3: heads {0,1}->kv0, {2,3}->kv1, {4,5}->kv2.
+    c = _rand_case(13, [6, 3], 2, hq=6, hk=3, d=8, nan=False)
+    v = c.v_pool.copy()
+    for kvh in range(3):
+        v[0, :, :, kvh] = _f16(np.full(8, float(kvh + 1)))
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], v[0], c.block_tables, c.seq_lens, c.scale)
+    for h in range(6):
+        np.testing.assert_allclose(out[:, h], h // 2 + 1.0, rtol=1e-14)
+
+
+def test_zero_length_row_is_all_zeros():
+    c = _rand_case(14, [0, 5, 0], 2)
+    out = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert np.all(np.isfinite(out[1]))
+
+
+# --- invariants fixed by the pages -------------------------------------------
+
+def test_output_invariant_under_permutation_of_physical_block_ids():
+    # blocks are interchangeable: moving every block to another id and
+    # rewriting the tables accordingly changes nothing, bit for bit.
+    c = _rand_case(15, [13, 7, 1, 20], 4, extra=5)
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(c.num_blocks)          # new id of old block b = perm[b]
+    kp = np.empty_like(c.k_pool[0]); vp = np.empty_like(c.v_pool[0])
+    kp[perm] = c.k_pool[0]; vp[perm] = c.v_pool[0]
+    bt = np.where(c.block_tables >= 0, perm[np.maximum(c.block_tables, 0)], -1).astype(np.int32)
+    a = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    b = oracle.paged_decode(c.q[0], kp, vp, bt, c.seq_lens, c.scale)
+    assert np.array_equal(a, b)
+
+
+def test_paged_equals_contiguous_slab():
+    c = wl.custom([1, 17, 64, 200], 16, seed=16, append=True, nan_fill=True)
+    kp, vp = oracle.paged_append(c.k_pool[0], c.v_pool[0], c.block_tables, c.positions,
+                                 c.k_new[0], c.v_new[0])
+    paged = oracle.paged_decode(c.q[0], kp, vp, c.block_tables, c.seq_lens, c.scale)
+    ks, vs = wl.padded_slab(c, 0, width=256, fill_bits=wl.FP16_NAN_BITS)
+    cont = oracle.contiguous_decode(c.q[0], ks, vs, c.seq_lens, c.scale)
+    assert np.all(np.isfinite(paged))
+    assert np.array_equal(paged, cont)
+
+
+def test_unread_slots_do_not_matter():
+    # NaN in every slot past each row's length (and in spare blocks) leaves the
+    # result finite and equal to the same rows with ordinary filler.
+    a = _rand_case(17, [3, 9, 16], 4, nan=True)
+    b = _rand_case(17, [3, 9, 16], 4, nan=False)
+    # same draws for the used tokens: copy used slots from a into b's pools
+    for r in range(a.rows):
+        for t in range(a.seq_lens[r]):
+            pb, s = a.block_tables[r, t // 4], t % 4
+            b.k_pool[0, pb, s] = a.k_pool[0, pb, s]
+            b.v_pool[0, pb, s] = a.v_pool[0, pb, s]
+    oa = oracle.paged_decode(a.q[0], a.k_pool[0], a.v_pool[0], a.block_tables, a.seq_lens, a.scale)
+    ob = oracle.paged_decode(a.q[0], b.k_pool[0], b.v_pool[0], a.block_tables, a.seq_lens, a.scale)
+    assert np.all(np.isfinite(oa))
+    assert np.array_equal(oa, ob)
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 64, 1000])
+def test_blockwise_logsumexp_merge_equals_single_pass(chunk):
+    c = wl.custom([1, 17, 64, 200], 16, seed=18, append=False, nan_fill=True)
+    single = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    merged, lse = oracle.blockwise_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables,
+                                          c.seq_lens, c.scale, chunk)
+    np.testing.assert_allclose(merged, single, rtol=1e-12, atol=1e-13)
+    # lse is log sum exp of the scores, pinned against scipy's logsumexp
+    r, h = 3, 7
+    kvh = h // (c.q_heads // c.kv_heads)
+    qv = oracle.half_to_double(c.q[0, r, h])
+    s = [c.scale * np.dot(qv, oracle.half_to_double(c.k_pool[0, c.block_tables[r, t // 16], t % 16, kvh]))
+         for t in range(c.seq_lens[r])]
+    assert abs(lse[r, h] - scipy.special.logsumexp(s)) < 1e-11
+
+
+def test_thread_count_does_not_change_results():
+    c = wl.custom([33, 7, 120, 64, 5], 16, seed=19, append=False, nan_fill=True)
+    a = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale, 1)
+    b = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale, 4)
+    assert np.array_equal(a, b)
+
+
+def test_bad_table_entry_is_an_error_not_a_read():
+    c = _rand_case(20, [5], 2)
+    bt = c.block_tables.copy()
+    bt[0, 1] = c.num_blocks  # out of range, and it is read (token 2..3)
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], bt, c.seq_lens, c.scale)
+    bt[0, 1] = -1
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], bt, c.seq_lens, c.scale)
+
+
+# --- append --------------------------------------------------------------------
+
+def test_golden_hand_worked_append():
+    g = json.load(open(os.path.join(GOLDEN, "append_hand.json")))
+    nb, bs, hk, d = g["num_blocks"], g["block_size"], g["kv_heads"], g["head_dim"]
+    kp = np.full((nb, bs, hk, d), wl.FP16_NAN_BITS, np.uint16)
+    vp = kp.copy()
+    k2, v2 = oracle.paged_append(kp, vp, np.array(g["block_tables"], np.int32),
+                                 np.array(g["positions"], np.int32), _f16(g["k_new"]), _f16(g["v_new"]))
+    ek, ev = kp.copy(), vp.copy()
+    for w in g["expected_writes"]:
+        ek[w["block"], w["slot"], 0] = _f16(w["k"])
+        ev[w["block"], w["slot"], 0] = _f16(w["v"])
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+
+
+def test_append_writes_only_the_target_slots():
+    c = wl.tiny(nan_fill=True)
+    kp, vp = oracle.paged_append(c.k_pool[0], c.v_pool[0], c.block_tables, c.positions,
+                                 c.k_new[0], c.v_new[0])
+    changed = np.argwhere(np.any(kp != c.k_pool[0], axis=(2, 3)))
+    expect = sorted((int(c.block_tables[r, p // 16]), int(p % 16)) for r, p in enumerate(c.positions))
+    assert sorted(map(tuple, changed.tolist())) == expect
+    for r, p in enumerate(c.positions):
+        pb = c.block_tables[r, p // 16]
+        assert np.array_equal(kp[pb, p % 16], c.k_new[0, r])
+        assert np.array_equal(vp[pb, p % 16], c.v_new[0, r])
+
+
+def test_append_position_beyond_table_is_an_error():
+    c = wl.custom([4], 4, seed=21, append=True, nan_fill=True)
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_append(c.k_pool[0], c.v_pool[0], c.block_tables, np.array([4], np.int32),
+                            c.k_new[0], c.v_new[0])
