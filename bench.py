@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark: paged decode attention (append + decode per layer) on one GB300.
+
+Workload (default): the mixed batch -- 32 rows, 31 lengths uniform on
+16..512 plus one 4096-token row, 64-token blocks, 12 query / 2 KV heads,
+head_dim 128, fp16, 28 layers each with its own pool, shuffled physical
+blocks, seed 0.  One step = for every layer, append the row's new token into
+its slot, then decode attention over the row's true length.  The step is one
+CUDA graph of 56 launches.
+
+Prints one JSON line (rank 0).  ``value`` is algorithmic bytes per step
+(KV + q + out + table + seq_lens + appended tokens) / device time per step,
+in GB/s.  ``roofline`` is for the decode kernel alone (a graph of 28 decode
+launches timed the same way) against the measured HBM copy bandwidth.
+``e2e`` repeats the step through the public API with per-step inputs copied
+from pinned host memory and outputs copied back inside the timed region.
+``cpu_baseline`` times the fp64 oracle on a bounded sample on the host cores.
+
+--impl reference times the oracle itself as the reference arm (rank 0 only).
+Multi-GPU runs (torchrun) are independent replicas: every rank runs the same
+workload on its own GPU (weak scaling), no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV GB/s and % of HBM roofline; rows·layers/s at batch 32"
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_LAYERS = 4
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["mixed", "uniform"], default="mixed")
+    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_06_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("decode") and name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """dram bytes per decode launch from a committed ncu summary, only if it was
+    taken on the current decode kernel source."""
+    p = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    if d.get("decode_source_hash") != decode_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def make_case(args):
+    from paged_kv_cache_06_gb300 import workloads as wl
+    if args.workload == "mixed":
+        return wl.mixed(seed=args.seed, layers=args.layers)
+    return wl.uniform(seed=args.seed, layers=args.layers)
+
+
+def workload_config(case, args):
+    from paged_kv_cache_06_gb300 import workloads as wl
+    b = wl.algorithmic_bytes(case)
+    desc = ("31 rows U{16..512} + 1 row of 4096" if args.workload == "mixed" else "32 rows x 1024")
+    return {
+        "workload": args.workload, "rows": case.rows, "layers": case.layers,
+        "lengths": desc, "tokens_per_layer": int(case.seq_lens.sum()),
+        "block_size": case.block_size, "q_heads": case.q_heads, "kv_heads": case.kv_heads,
+        "head_dim": case.head_dim, "seed": args.seed,
+        "step": "per layer: paged_kv_append then paged_attention_decode (CUDA graph)",
+        "bytes_per_step": case.layers * (b["decode_layer"] + b["append_layer"]),
+        "l2": f"inputs larger than L2: {case.layers * b['kv_logical'] / 1e6:.0f} MB of KV per step "
+              "vs 129 MB L2, each layer its own pool",
+        "parallelism": "replicas",
+    }
+
+
+def cpu_oracle_sample(case, layers: int):
+    """Time the fp64 oracle on the first ``layers`` layers (append + decode)."""
+    import oracle
+    from paged_kv_cache_06_gb300 import workloads as wl
+    threads = oracle.default_threads()
+    b = wl.algorithmic_bytes(case)
+    t0 = time.perf_counter()
+    for l in range(layers):
+        kp, vp = oracle.paged_append(case.k_pool[l], case.v_pool[l], case.block_tables,
+                                     case.positions, case.k_new[l], case.v_new[l])
+        oracle.paged_decode(case.q[l], kp, vp, case.block_tables, case.seq_lens, case.scale,
+                            num_threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = layers * (b["decode_layer"] + b["append_layer"])
+    return nbytes / dt / 1e9, threads, dt
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, pg):
+    import torch
+    from paged_kv_cache_06_gb300 import ops
+    from paged_kv_cache_06_gb300 import workloads as wl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ops.lib()  # fails loudly if the CUDA library cannot be built or loaded
+    case = make_case(args)
+    b = wl.algorithmic_bytes(case)
+    d = wl.to_device(case, dev)
+    L = case.layers
+    rows, hq, hk, hd = case.rows, case.q_heads, case.kv_heads, case.head_dim
+    msl = case.max_seq_len
+    ws = ops.alloc_workspace(rows, hq, hk, hd, msl, case.block_size, device=dev)
+    out = torch.zeros(L, rows, hq, hd, dtype=torch.float16, device=dev)
+
+    def step():
+        for l in range(L):
+            ops.append(d["k_pool"][l], d["v_pool"][l], d["block_tables"], d["positions"],
+                       d["k_new"][l], d["v_new"][l])
+            ops.decode(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l], d["block_tables"],
+                       d["seq_lens"], case.scale, msl, ws)
+
+    def decode_only():
+        for l in range(L):
+            ops.decode(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l], d["block_tables"],
+                       d["seq_lens"], case.scale, msl, ws)
+
+    def capture(fn):
+        fn()  # eager warm-up (also validates arguments)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(g, k, w, clocks=None):
+        for _ in range(w):
+            g.replay()
+        barrier(pg)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        cl = clocks.stop() if clocks else None
+        barrier(pg)
+        return e0.elapsed_time(e1) / k, cl
+
+    g_step = capture(step)
+    clocks = ClockSampler(torch.cuda.current_device())
+    ms_local, clk = time_graph(g_step, args.steps, args.warmup, clocks)
+    ms = max_over_ranks(pg, ms_local)
+    bytes_step = L * (b["decode_layer"] + b["append_layer"])
+    total_bytes = sum_over_ranks(pg, bytes_step)
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    # Decode kernel alone: 28 back-to-back launches, same timing rules.
+    g_dec = capture(decode_only)
+    ms_dec, _ = time_graph(g_dec, args.steps, args.warmup)
+    per_launch_s = ms_dec * 1e-3 / L
+    achieved = b["decode_layer"] / per_launch_s / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = load_traffic(args.workload)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) fp16 values, seeded lengths and block permutation)",
+        "config": workload_config(case, args),
+        "rows_layers_per_s": round(world * rows * L / (ms * 1e-3), 1),
+        "rows_heads_per_s": round(world * rows * hq * L / (ms * 1e-3), 1),
+        "hbm_frac_of_measured": round(value / world / peak, 4),
+        "hbm_frac_of_nominal_8TBs": round(value / world / 8000.0, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": "paged_attention_decode",
+                     "bytes_per_launch": b["decode_layer"],
+                     "launch_us": round(per_launch_s * 1e6, 3)},
+        "gpu_launches": args.steps * L * 2,
+        "clocks": clk,
+    }
+
+    # Padded comparator: the same rows in a [rows][4096] slab, full width read.
+    if not args.no_comparator and args.workload == "mixed":
+        width = int(case.seq_lens.max())
+        slabs = []
+        for l in range(L):
+            ks, vs = wl.padded_slab(case, l, width=width, fill_bits=0)
+            slabs.append((torch.from_numpy(ks.view(np.float16)).to(dev),
+                          torch.from_numpy(vs.view(np.float16)).to(dev)))
+        wsp = ops.alloc_workspace(rows, hq, hk, hd, width, case.block_size, device=dev)
+
+        def padded():
+            for l in range(L):
+                ops.padded_decode(out[l], d["q"][l], slabs[l][0], slabs[l][1], d["seq_lens"],
+                                  case.scale, wsp)
+
+        g_pad = capture(padded)
+        ms_pad, _ = time_graph(g_pad, args.steps, args.warmup)
+        result["comparator"] = {
+            "padded_decode_ms_per_step": round(ms_pad, 5),
+            "paged_decode_ms_per_step": round(ms_dec, 5),
+            "paged_speedup": round(ms_pad / ms_dec, 3),
+            "padded_bytes_read_per_layer": rows * width * hk * hd * 2 * 2,
+        }
+        del slabs, g_pad
+
+    # End to end through the public API: per-step inputs from pinned host memory.
+    if not args.no_e2e:
+        h_q = torch.empty_like(d["q"], device="cpu").pin_memory()
+        h_kn = torch.empty_like(d["k_new"], device="cpu").pin_memory()
+        h_vn = torch.empty_like(d["v_new"], device="cpu").pin_memory()
+        h_bt = torch.empty_like(d["block_tables"], device="cpu").pin_memory()
+        h_sl = torch.empty_like(d["seq_lens"], device="cpu").pin_memory()
+        h_pos = torch.empty_like(d["positions"], device="cpu").pin_memory()
+        h_out = torch.empty_like(out, device="cpu").pin_memory()
+        for h, src in ((h_q, d["q"]), (h_kn, d["k_new"]), (h_vn, d["v_new"]),
+                       (h_bt, d["block_tables"]), (h_sl, d["seq_lens"]), (h_pos, d["positions"])):
+            h.copy_(src)
+        ins = ((d["q"], h_q), (d["k_new"], h_kn), (d["v_new"], h_vn), (d["block_tables"], h_bt),
+               (d["seq_lens"], h_sl), (d["positions"], h_pos))
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for dst, src in ins:
+                dst.copy_(src, non_blocking=True)
+            g_step.replay()
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier(pg)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms_e2e = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps)
+        result["e2e"] = {"value": round(total_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": round(ms_e2e, 5)}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, threads, dt = cpu_oracle_sample(case, min(CPU_SAMPLE_LAYERS, L))
+        result["cpu_baseline"] = {
+            "value": round(gbs, 5), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {min(CPU_SAMPLE_LAYERS, L)} of {L} layers of the same workload "
+                      f"(append + decode, fp64 C, OpenMP), {dt:.2f} s"}
+    return result
+
+
+def run_reference(args, rank, world, pg):
+    """The oracle as the reference arm: rank 0 only, on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_cache_06_gb300 import workloads as wl
+    oracle.build()
+    case = make_case(args)
+    layers = min(CPU_SAMPLE_LAYERS, case.layers)
+    b = wl.algorithmic_bytes(case)
+    threads = oracle.default_threads()
+
+    def step():
+        for l in range(layers):
+            kp, vp = oracle.paged_append(case.k_pool[l], case.v_pool[l], case.block_tables,
+                                         case.positions, case.k_new[l], case.v_new[l])
+            oracle.paged_decode(case.q[l], kp, vp, case.block_tables, case.seq_lens, case.scale,
+                                num_threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    nbytes = layers * (b["decode_layer"] + b["append_layer"])
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"each step: first {layers} of {case.layers} layers of the workload "
+              f"(append + decode), fp64 C oracle, OpenMP")
+    cfg = workload_config(case, args)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) fp16 values, seeded lengths and block permutation)",
+        "config": cfg,
+        "rows_layers_per_s": round(case.rows * layers / (ms * 1e-3), 2),
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # Rank 0 alone times the oracle; other ranks exit without work.
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world, None)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, pg = dist_setup(args)
+    res = run_ours(args, rank, world, pg)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+/*
+ * paged_kv.h -- C ABI of libpagedkv: paged KV-cache append and decode
+ * attention for GB300 (sm_103a), plus a host-side block manager.
+ *
+ * Terms (from the pages this library implements):
+ *   - "PagedAttention" (deepconcepts.dev), section "PagedAttention": the KV
+ *     cache is cut into fixed-size blocks; each sequence keeps a block table
+ *     mapping its logical block n to the physical block holding it, and the
+ *     attention kernel walks that table instead of striding a slab.
+ *     Section "What the block table costs": the table is one dense int32
+ *     array [max_num_reqs][max_num_blocks_per_req].
+ *   - "Paged attention" (danielfleming.xyz), section "What changed": decode
+ *     reads, per row, only the blocks its table lists, at the row's own
+ *     length; a free list hands blocks out at admission (reserve on admit).
+ *   - "SLM paged attention" (aicassindra.com), section "The architecture":
+ *     one pre-allocated pool sliced into equal blocks; logical block =
+ *     position / block_size; the last block fills slot by slot; shared
+ *     prefix blocks carry a reference count and are copied on write.
+ *
+ * Data layout (all device buffers, row-major, contiguous, 16-byte aligned):
+ *   k_pool, v_pool   fp16 [num_blocks][block_size][kv_heads][head_dim]
+ *   block_tables     int32 [rows][max_blocks_per_row]; entries past a row's
+ *                    ceil(seq_len / block_size) are never read (-1 by
+ *                    convention)
+ *   seq_lens         int32 [rows]: tokens a row attends to, including the
+ *                    token appended in this step
+ *   q, out           fp16 [rows][q_heads][head_dim]
+ *   k_new, v_new     fp16 [rows][kv_heads][head_dim]
+ * Query head h reads KV head h / (q_heads / kv_heads) (contiguous groups).
+ *
+ * Ownership: the caller allocates and owns every buffer (including the
+ * decode workspace).  The library never allocates, frees or synchronises,
+ * except pkv_check_error, which synchronises the given stream to read the
+ * device error word.
+ *
+ * Asynchrony: kernel entry points enqueue work on `stream` and return.
+ *
+ * Errors: every call returns a pkv_status.  Problems visible on the host
+ * (null pointers, bad sizes, unsupported shapes, small workspace) are
+ * returned before anything is launched.  Problems only visible on the device
+ * (a table entry outside [0, num_blocks), a seq_len above the bound, an
+ * append position past the row's table) never fault: the offending block,
+ * row or token is skipped, and when `dev_err` is non-null a PKV_DEV_ERR_*
+ * bit is OR-ed into *dev_err.  Kernels never trap and never spin-wait.
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,  /* null pointer, negative/zero size, bad combination */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, group > 8, ... */
+    PKV_ERR_WORKSPACE = 3,    /* workspace null or smaller than required */
+    PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    PKV_ERR_BAD_TABLE = 5,    /* (block manager) inconsistent table / id */
+    PKV_ERR_NO_BLOCKS = 6,    /* (block manager) free list cannot cover the request */
+    PKV_ERR_NOT_FOUND = 7,    /* (block manager) unknown sequence or prefix id */
+    PKV_ERR_STATE = 8         /* (block manager) operation not valid in this state */
+} pkv_status;
+
+/* Bits OR-ed into the optional device error word. */
+#define PKV_DEV_ERR_BLOCK_ID 0x1 /* a table entry that had to be read is outside [0, num_blocks) */
+#define PKV_DEV_ERR_SEQ_LEN 0x2  /* seq_len < 0, > max_seq_len or > max_blocks_per_row * block_size */
+#define PKV_DEV_ERR_POSITION 0x4 /* append position's logical block >= max_blocks_per_row */
+
+/* Human-readable name of a pkv_status.  Never null; static storage. */
+const char* pkv_status_string(int status);
+
+/* ABI version of this header (increments on incompatible changes). */
+int pkv_abi_version(void);
+
+/*
+ * paged_kv_append -- write this step's new K and V token of every row into
+ * its slot.  Defining passage: "SLM paged attention", section "The
+ * architecture" (logical block = position / block_size; the last block's
+ * slots fill one at a time; growth is one block at a time).
+ *
+ * For each row r with positions[r] >= 0, with lb = positions[r] / block_size,
+ * off = positions[r] % block_size and pb = block_tables[r][lb]:
+ *     k_pool[pb][off][h][:] = k_new[r][h][:]   and likewise for V,
+ * for every KV head h.  Rows with positions[r] < 0 are skipped.  The copy is
+ * bit-exact.  Two rows naming the same slot is a caller error (the result is
+ * one of the two writes).  lb >= max_blocks_per_row sets
+ * PKV_DEV_ERR_POSITION, pb outside [0, num_blocks) sets PKV_DEV_ERR_BLOCK_ID;
+ * either way that row is skipped.
+ *
+ * head_dim must be a multiple of 8; rows may be 0 (nothing is launched).
+ */
+int paged_kv_append(void* k_pool, void* v_pool, const int32_t* block_tables,
+                    const int32_t* positions, const void* k_new, const void* v_new,
+                    int rows, int kv_heads, int head_dim, int block_size,
+                    int max_blocks_per_row, int num_blocks, int32_t* dev_err,
+                    cudaStream_t stream);
+
+/*
+ * paged_attention_workspace_size -- bytes of device workspace that
+ * paged_attention_decode needs for these sizes (the split-K partial results
+ * and per-row arrival counters).  Pure host arithmetic; never fails (returns
+ * 0 for invalid sizes).  max_seq_len is the caller's upper bound on every
+ * seq_lens[r] of the calls the workspace will serve.
+ *
+ * The workspace must be zero-filled once after allocation.  Every decode
+ * call leaves it ready for the next call (its counters back at zero), so it
+ * may be reused by later calls on the same stream, including from a CUDA
+ * graph; two decode calls that run at the same time need separate
+ * workspaces.
+ */
+size_t paged_attention_workspace_size(int rows, int q_heads, int kv_heads, int head_dim,
+                                      int max_seq_len, int block_size);
+
+/*
+ * paged_attention_decode -- one decode step of attention over a paged KV
+ * cache.  Defining passages: "PagedAttention" (deepconcepts.dev), sections
+ * "PagedAttention" and "What the block table costs" (walk the table, gather
+ * the listed blocks) and its closing note on FlashAttention (block-wise
+ * softmax recombined exactly); "Paged attention" (danielfleming.xyz),
+ * section "What changed" (read each row only at its true length).
+ *
+ * For every row r and query head h, with L = seq_lens[r],
+ * kvh = h / (q_heads / kv_heads) and, for t < L,
+ * K_t = k_pool[block_tables[r][t / block_size]][t % block_size][kvh][:]:
+ *     out[r][h][:] = sum_t softmax_t(scale * q[r][h] . K_t) * V_t[:]
+ * computed in fp32 and rounded to fp16 (round to nearest even).  Rows with
+ * L == 0 produce zeros.  Long rows are split across thread blocks and the
+ * partial results merged exactly through their log-sum-exp.
+ *
+ * Supported: head_dim == 128; q_heads % kv_heads == 0 with group size
+ * q_heads / kv_heads <= 8; block_size in [1, 1024]; max_seq_len <=
+ * max_blocks_per_row * block_size.  Anything else returns
+ * PKV_ERR_UNSUPPORTED or PKV_ERR_INVALID_ARG before launch.
+ * workspace must hold paged_attention_workspace_size(...) bytes (see there).
+ * seq_lens[r] > max_seq_len is clamped to max_seq_len and flagged
+ * (PKV_DEV_ERR_SEQ_LEN); bad table entries are skipped and flagged.
+ */
+int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, const int32_t* seq_lens, int rows,
+                           int q_heads, int kv_heads, int head_dim, int block_size, float scale,
+                           int max_blocks_per_row, int num_blocks, int max_seq_len,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                           cudaStream_t stream);
+
+/*
+ * paged_attention_padded_decode -- the comparator the paged cache replaced:
+ * attention over a contiguous slab with one full-width slot per row, computed
+ * across the whole width for every row with columns past the row's length
+ * masked out ("Continuous batching", danielfleming.xyz, sections "What
+ * changed" and "Where the missing capacity went": the mask hides the data but
+ * not the work).  Used to measure what reading true lengths saves.
+ *
+ * k_slab, v_slab: fp16 [rows][width][kv_heads][head_dim].  Row r's result
+ * equals paged_attention_decode's on the same tokens; every column of the
+ * slab is read.  Masked columns must hold finite values.  workspace as for
+ * paged_attention_decode with max_seq_len = width.
+ */
+int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
+                                  const void* v_slab, const int32_t* seq_lens, int rows,
+                                  int width, int q_heads, int kv_heads, int head_dim,
+                                  float scale, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * pkv_check_error -- synchronise `stream`, copy the device error word to
+ * *host_err and clear it on the device.  Returns PKV_ERR_CUDA if the stream
+ * reported an error.  The only library call that blocks.
+ */
+int pkv_check_error(int32_t* dev_err, cudaStream_t stream, int32_t* host_err);
+
+/* ------------------------------------------------------------------------ */
+/*
+ * Host block manager.  Defining passages: "Paged attention"
+ * (danielfleming.xyz), section "What changed" (a free list hands out blocks
+ * at admission and takes them back at eviction with no copy; reserve on
+ * admit: admit only if every block for prompt + full budget is free);
+ * "SLM paged attention", section "The architecture" and "End-to-end flow"
+ * (O(1) pop/push free list; growth one block at a time when nothing was
+ * reserved; shared prefix blocks are reference counted, freed at count 0 and
+ * copied on the first write into them); "PagedAttention" (deepconcepts.dev),
+ * section "So what does block_size trade?" (blocks are shared whole: only
+ * floor(prefix_tokens / block_size) blocks of a prefix are shareable).
+ *
+ * Host memory only, single-threaded (callers serialise access).  Block ids
+ * are in [0, num_blocks).  Errors: PKV_ERR_INVALID_ARG for bad arguments,
+ * PKV_ERR_NOT_FOUND for unknown ids, PKV_ERR_NO_BLOCKS when the free list
+ * cannot cover a request (state unchanged: nothing is partially allocated),
+ * PKV_ERR_STATE for a sequence that is already admitted / past its table.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+typedef struct {
+    int32_t num_blocks;      /* pool size */
+    int32_t free_blocks;     /* on the free list */
+    int32_t used_blocks;     /* num_blocks - free_blocks */
+    int32_t shared_blocks;   /* used blocks with reference count > 1 */
+    int32_t sequences;       /* admitted sequences */
+    int32_t prefixes;        /* registered prefixes */
+    int64_t live_tokens;     /* sum of sequence lengths */
+    int64_t reserved_slots;  /* slots held by sequences but not yet written */
+    int64_t cow_copies;      /* copy-on-write events so far */
+} pkv_bm_stats_t;
+
+/* Create a manager over a pool of num_blocks blocks of block_size tokens;
+ * tables have max_blocks_per_row entries.  All blocks start free. */
+int pkv_bm_create(int num_blocks, int block_size, int max_blocks_per_row,
+                  pkv_block_manager** out);
+void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Register a shared prefix of prefix_tokens tokens: takes
+ * floor(prefix_tokens / block_size) blocks from the free list (the partial
+ * remainder is not shareable) and holds one reference on each.  Writes the
+ * prefix id and (nullable) the block ids, in logical order, to block_ids_out
+ * (capacity floor(prefix_tokens / block_size)). */
+int pkv_bm_register_prefix(pkv_block_manager* bm, int prefix_tokens, int32_t* prefix_id_out,
+                           int32_t* block_ids_out);
+/* Drop the registration's own reference; blocks return to the free list once
+ * no sequence references them. */
+int pkv_bm_release_prefix(pkv_block_manager* bm, int32_t prefix_id);
+
+/* Admit sequence seq_id with prompt_len tokens and a budget of up to
+ * max_new_tokens further tokens.  With reserve != 0 (reserve on admit) every
+ * block the sequence can ever need -- ceil((prompt_len + max_new_tokens) /
+ * block_size) table entries, including the private copy a later write into a
+ * shared block needs -- is taken now, or nothing is and PKV_ERR_NO_BLOCKS is
+ * returned.  With reserve == 0 only the prompt's blocks are taken and later
+ * blocks come one at a time from pkv_bm_append_slot.  prefix_id >= 0 points
+ * the sequence's leading entries at that prefix's shared blocks (as many as
+ * its prompt covers). */
+int pkv_bm_admit(pkv_block_manager* bm, int64_t seq_id, int prompt_len, int max_new_tokens,
+                 int32_t prefix_id, int reserve);
+
+/* Claim the slot for the sequence's next token and advance its length by
+ * one.  Writes the token's position to *position_out.  If that position
+ * lies in a block the sequence shares, the block is copied on write: a
+ * private block is taken (from the reservation, else the free list), the
+ * table entry is repointed, and the copy the caller must perform on the
+ * device is reported in *cow_src_out / *cow_dst_out (both -1 when no copy is
+ * needed).  Returns PKV_ERR_NO_BLOCKS (length unchanged) if a new block is
+ * needed and none is free, PKV_ERR_STATE past max_blocks_per_row. */
+int pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int32_t* position_out,
+                       int32_t* cow_src_out, int32_t* cow_dst_out);
+
+/* Release a finished sequence: every block it references loses one
+ * reference; blocks at zero go back to the free list (no data moves). */
+int pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+
+/* Copy the sequence's table (max_blocks_per_row int32, -1 past its blocks)
+ * into row_out and its length into *seq_len_out (nullable). */
+int pkv_bm_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* row_out,
+                 int32_t* seq_len_out);
+
+/* Pool and sharing counters (the pages' operating metrics: memory in use,
+ * blocks shared). */
+int pkv_bm_stats(const pkv_block_manager* bm, pkv_bm_stats_t* out);
+
+/* Reference count of a physical block (0 = free). */
+int pkv_bm_refcount(const pkv_block_manager* bm, int32_t block_id, int32_t* count_out);
+
+/* Host-side fault injection for tests: after `pops` more successful block
+ * pops, every further pop fails as if the free list were empty (-1 turns it
+ * off). */
+int pkv_bm_inject_pop_failure(pkv_block_manager* bm, int pops);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H */

@@ -1,0 +1,183 @@
+"""Thin ctypes binding over libpagedkv's C ABI (include/paged_kv.h).
+
+Argument marshalling only: each function checks the tensors' device, dtype
+and contiguity, derives the sizes from their shapes and calls the C entry
+point of the same name with raw pointers and the current CUDA stream.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+fallback, and calling an op without the built library raises.
+
+Tensors (torch, on the GPU):
+  k_pool, v_pool  fp16 [num_blocks][block_size][kv_heads][head_dim]
+  block_tables    int32 [rows][max_blocks_per_row]
+  seq_lens        int32 [rows];  positions int32 [rows]
+  q, out          fp16 [rows][q_heads][head_dim]
+  k_new, v_new    fp16 [rows][kv_heads][head_dim]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+PKV_OK = 0
+STATUS_NAMES = {}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpagedkv.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libpagedkv.so missing at {path}")
+            L = ctypes.CDLL(path)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L: ctypes.CDLL) -> None:
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.pkv_status_string.argtypes = [I]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_abi_version.argtypes = []
+    L.pkv_abi_version.restype = I
+    L.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    L.paged_kv_append.restype = I
+    L.paged_attention_workspace_size.argtypes = [I, I, I, I, I, I]
+    L.paged_attention_workspace_size.restype = S
+    L.paged_attention_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P, S, P, P]
+    L.paged_attention_decode.restype = I
+    L.paged_attention_padded_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, S, P, P]
+    L.paged_attention_padded_decode.restype = I
+    L.pkv_check_error.argtypes = [P, P, P]
+    L.pkv_check_error.restype = I
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PKV_OK:
+        raise PagedKVError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _need_err(dev_err: Optional[torch.Tensor]) -> None:
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, 1)
+
+
+def append(k_pool, v_pool, block_tables, positions, k_new, v_new, dev_err=None, stream=None):
+    """paged_kv_append: write each row's new token into its slot."""
+    for t, n, dt, nd in ((k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (positions, "positions", torch.int32, 1),
+                         (k_new, "k_new", torch.float16, 3), (v_new, "v_new", torch.float16, 3)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    nb, bs, hk, d = k_pool.shape
+    rows = positions.shape[0]
+    st = lib().paged_kv_append(_ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(positions),
+                               _ptr(k_new), _ptr(v_new), rows, hk, d, bs, block_tables.shape[1], nb,
+                               _ptr(dev_err), _stream(stream))
+    _check("paged_kv_append", st)
+
+
+def workspace_size(rows: int, q_heads: int, kv_heads: int, head_dim: int, max_seq_len: int,
+                   block_size: int) -> int:
+    return int(lib().paged_attention_workspace_size(rows, q_heads, kv_heads, head_dim, max_seq_len,
+                                                    block_size))
+
+
+def alloc_workspace(rows, q_heads, kv_heads, head_dim, max_seq_len, block_size, device="cuda"):
+    """Zero-filled workspace of the size the C ABI asks for."""
+    n = workspace_size(rows, q_heads, kv_heads, head_dim, max_seq_len, block_size)
+    if n == 0:
+        raise ValueError("unsupported sizes for paged_attention_decode")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale: float, max_seq_len: int,
+           workspace, dev_err=None, stream=None):
+    """paged_attention_decode: attention of each row's query over its paged tokens."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                      _ptr(block_tables), _ptr(seq_lens), rows, hq, hk, d, bs,
+                                      float(scale), block_tables.shape[1], nb, int(max_seq_len),
+                                      _ptr(workspace), workspace.numel(), _ptr(dev_err),
+                                      _stream(stream))
+    _check("paged_attention_decode", st)
+
+
+def padded_decode(out, q, k_slab, v_slab, seq_lens, scale: float, workspace, dev_err=None,
+                  stream=None):
+    """paged_attention_padded_decode: the full-width masked comparator."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_slab, "k_slab", torch.float16, 4), (v_slab, "v_slab", torch.float16, 4),
+                         (seq_lens, "seq_lens", torch.int32, 1),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    _, width, hk, _ = k_slab.shape
+    st = lib().paged_attention_padded_decode(_ptr(out), _ptr(q), _ptr(k_slab), _ptr(v_slab),
+                                             _ptr(seq_lens), rows, width, hq, hk, d, float(scale),
+                                             _ptr(workspace), workspace.numel(), _ptr(dev_err),
+                                             _stream(stream))
+    _check("paged_attention_padded_decode", st)
+
+
+def check_error(dev_err: torch.Tensor, stream=None) -> int:
+    """Synchronise, read and clear the device error word (PKV_DEV_ERR_* bits)."""
+    _need(dev_err, "dev_err", torch.int32, 1)
+    host = ctypes.c_int32(0)
+    st = lib().pkv_check_error(_ptr(dev_err), _stream(stream), ctypes.byref(host))
+    _check("pkv_check_error", st)
+    return int(host.value)

@@ -361,3 +361,29 @@ def algorithmic_bytes(case: DecodeCase) -> Dict[str, int]:
         "decode_layer_unique": kv_unique + qo + table,
         "append_layer": append,
     }
+
+
+def to_device(case: DecodeCase, device="cuda") -> Dict[str, "torch.Tensor"]:
+    """Copy a case's arrays to the device as fp16 / int32 torch tensors."""
+    def f16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).to(device)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+    return {
+        "q": f16(case.q), "k_pool": f16(case.k_pool), "v_pool": f16(case.v_pool),
+        "k_new": f16(case.k_new), "v_new": f16(case.v_new),
+        "block_tables": i32(case.block_tables), "seq_lens": i32(case.seq_lens),
+        "positions": i32(case.positions),
+    }
+
+
+def row_subset(case: DecodeCase, rows) -> DecodeCase:
+    """The same case restricted to some rows (pools unchanged)."""
+    rows = np.asarray(rows)
+    return dataclasses.replace(case, seq_lens=case.seq_lens[rows].copy(),
+                               positions=case.positions[rows].copy(),
+                               block_tables=case.block_tables[rows].copy(),
+                               q=case.q[:, rows].copy(), k_new=case.k_new[:, rows].copy(),
+                               v_new=case.v_new[:, rows].copy())
