@@ -166,6 +166,43 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
                                   float scale, void* workspace, size_t workspace_bytes,
                                   int32_t* dev_err, cudaStream_t stream);
 
+/* Bytes of the static device scratch behind paged_attention_decode_noalloc
+ * (8 MiB, held by every GPU that loads the library until the process exits). */
+#define PKV_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)
+
+/*
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that
+ * cannot allocate device memory, such as a plug-in inside a host framework
+ * that owns all device memory through its own pool, or a serving loop that
+ * forbids cudaMalloc after start-up because cudaMalloc / cudaFree can
+ * synchronise the device and stall other streams.  (The pages have no
+ * counterpart: this is an interface choice of this library.)
+ *
+ * Same arguments, layout and result as paged_attention_decode, minus the
+ * workspace: the caller still passes every input and output buffer, and the
+ * split-K scratch comes from one file-scope static device array of
+ * PKV_NOALLOC_WORKSPACE_BYTES instead.  Allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ *
+ *  - Limit: sizes whose paged_attention_workspace_size(...) exceeds
+ *    PKV_NOALLOC_WORKSPACE_BYTES return PKV_ERR_WORKSPACE before launch.
+ *  - Set-up: the first call made on a device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches it;
+ *    make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    last call's contents.  Each call first clears the part that must start
+ *    at zero (the per-row arrival counters, by cudaMemsetAsync on `stream`);
+ *    the rest is written before it is read.  Calls that overlap on the GPU
+ *    (for example on two streams at once) race on the array and give wrong
+ *    results: serialise them.
+ */
+int paged_attention_decode_noalloc(void* out, const void* q, const void* k_pool,
+                                   const void* v_pool, const int32_t* block_tables,
+                                   const int32_t* seq_lens, int rows, int q_heads, int kv_heads,
+                                   int head_dim, int block_size, float scale,
+                                   int max_blocks_per_row, int num_blocks, int max_seq_len,
+                                   int32_t* dev_err, cudaStream_t stream);
+
 /*
  * pkv_check_error -- synchronise `stream`, copy the device error word to
  * *host_err and clear it on the device.  Returns PKV_ERR_CUDA if the stream

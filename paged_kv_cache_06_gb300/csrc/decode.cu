@@ -223,18 +223,27 @@ static int check_heads(int q_heads, int kv_heads, int head_dim) {
     return PKV_OK;
 }
 
-static DecodeParams make_params(void* out, const void* q, const void* k, const void* v, int rows,
-                                int q_heads, int kv_heads, float scale, int nsplit_max,
-                                void* workspace, int32_t* dev_err) {
+static DecodeParams make_params(void* out, const void* q, const void* k, const void* v,
+                                const int32_t* tables, const int32_t* seq_lens, int rows,
+                                int q_heads, int kv_heads, int block_size, int mbpr, int nb,
+                                int limit, int width, float scale, int nsplit_max, void* workspace,
+                                int32_t* dev_err) {
     DecodeParams p{};
     p.out = static_cast<__half*>(out);
     p.q = static_cast<const __half*>(q);
     p.k = static_cast<const __half*>(k);
     p.v = static_cast<const __half*>(v);
+    p.tables = tables;
+    p.seq_lens = seq_lens;
     p.rows = rows;
     p.hq = q_heads;
     p.hk = kv_heads;
     p.group = q_heads / kv_heads;
+    p.bs = block_size;
+    p.mbpr = mbpr;
+    p.nb = nb;
+    p.limit = limit;
+    p.width = width;
     p.nsplit_max = nsplit_max;
     p.scale_log2 = scale * kLog2e;
     const WorkspaceLayout w = workspace_layout(rows, q_heads, nsplit_max);
@@ -247,6 +256,15 @@ static DecodeParams make_params(void* out, const void* q, const void* k, const v
     return p;
 }
 
+}  // namespace pkv
+
+namespace pkv {
+// Leading bytes of a decode workspace that must be zero when a call starts
+// (the per-row arrival counters); everything after them is written before it
+// is read.
+size_t decode_workspace_zero_bytes(int rows) {
+    return rows <= 0 ? 0 : workspace_layout(rows, 1, 1).m;
+}
 }  // namespace pkv
 
 extern "C" size_t paged_attention_workspace_size(int rows, int q_heads, int kv_heads, int head_dim,
@@ -279,15 +297,10 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_po
     const int nsplit = splits_for(max_seq_len);
     if (!workspace || workspace_bytes < workspace_layout(rows, q_heads, nsplit).total)
         return PKV_ERR_WORKSPACE;
-    DecodeParams p = make_params(out, q, k_pool, v_pool, rows, q_heads, kv_heads, scale, nsplit,
-                                 workspace, dev_err);
-    p.tables = block_tables;
-    p.seq_lens = seq_lens;
-    p.bs = block_size;
-    p.mbpr = max_blocks_per_row;
-    p.nb = num_blocks;
-    p.limit = max_seq_len;
-    p.width = 0;
+    const DecodeParams p = make_params(out, q, k_pool, v_pool, block_tables, seq_lens, rows,
+                                       q_heads, kv_heads, block_size, max_blocks_per_row,
+                                       num_blocks, max_seq_len, 0, scale, nsplit, workspace,
+                                       dev_err);
     decode_split_kernel<true><<<dim3(nsplit, rows), kThreads, 0, stream>>>(p);
     return launch_status();
 }
@@ -309,10 +322,9 @@ extern "C" int paged_attention_padded_decode(void* out, const void* q, const voi
     const int nsplit = splits_for(width);
     if (!workspace || workspace_bytes < workspace_layout(rows, q_heads, nsplit).total)
         return PKV_ERR_WORKSPACE;
-    DecodeParams p = make_params(out, q, k_slab, v_slab, rows, q_heads, kv_heads, scale, nsplit,
-                                 workspace, dev_err);
-    p.limit = width;
-    p.width = width;
+    const DecodeParams p = make_params(out, q, k_slab, v_slab, nullptr, seq_lens, rows, q_heads,
+                                       kv_heads, 1, 1, 1, width, width, scale, nsplit, workspace,
+                                       dev_err);
     decode_split_kernel<false><<<dim3(nsplit, rows), kThreads, 0, stream>>>(p);
     return launch_status();
 }

@@ -36,4 +36,7 @@ inline int launch_status() {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bytes at the start of a decode workspace that must be zero before a call.
+size_t decode_workspace_zero_bytes(int rows);
+
 }  // namespace pkv

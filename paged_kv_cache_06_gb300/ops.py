@@ -67,6 +67,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_padded_decode.restype = I
     L.pkv_check_error.argtypes = [P, P, P]
     L.pkv_check_error.restype = I
+    L.paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P, P]
+    L.paged_attention_decode_noalloc.restype = I
 
 
 def status_string(status: int) -> str:
@@ -172,6 +174,25 @@ def padded_decode(out, q, k_slab, v_slab, seq_lens, scale: float, workspace, dev
                                              _ptr(workspace), workspace.numel(), _ptr(dev_err),
                                              _stream(stream))
     _check("paged_attention_padded_decode", st)
+
+
+def decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale: float,
+                   max_seq_len: int, dev_err=None, stream=None):
+    """paged_attention_decode_noalloc: decode with the library's static scratch
+    (for callers that cannot allocate a workspace; see include/paged_kv.h)."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                              _ptr(block_tables), _ptr(seq_lens), rows, hq, hk, d,
+                                              bs, float(scale), block_tables.shape[1], nb,
+                                              int(max_seq_len), _ptr(dev_err), _stream(stream))
+    _check("paged_attention_decode_noalloc", st)
 
 
 def check_error(dev_err: torch.Tensor, stream=None) -> int:
