@@ -70,6 +70,7 @@ typedef enum {
 #define PKV_DEV_ERR_BLOCK_ID 0x1 /* a table entry that had to be read is outside [0, num_blocks) */
 #define PKV_DEV_ERR_SEQ_LEN 0x2  /* seq_len < 0, > max_seq_len or > max_blocks_per_row * block_size */
 #define PKV_DEV_ERR_POSITION 0x4 /* append position's logical block >= max_blocks_per_row */
+#define PKV_DEV_ERR_TIMEOUT 0x8  /* a bounded wait inside a kernel gave up (the call's output is invalid) */
 
 /* Human-readable name of a pkv_status.  Never null; static storage. */
 const char* pkv_status_string(int status);

@@ -260,18 +260,23 @@ static DecodeParams make_params(void* out, const void* q, const void* k, const v
 
 namespace pkv {
 // Leading bytes of a decode workspace that must be zero when a call starts
-// (the per-row arrival counters); everything after them is written before it
-// is read.
-size_t decode_workspace_zero_bytes(int rows) {
-    return rows <= 0 ? 0 : workspace_layout(rows, 1, 1).m;
+// (the arrival counters); everything after them is written before it is read.
+size_t decode_workspace_zero_bytes(int rows, int q_heads, int kv_heads, int head_dim,
+                                   int max_seq_len, int block_size) {
+    if (rows <= 0) return 0;
+    if (tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size))
+        return tma_workspace_zero_bytes(rows, kv_heads, max_seq_len);
+    return workspace_layout(rows, 1, 1).m;
 }
 }  // namespace pkv
 
 extern "C" size_t paged_attention_workspace_size(int rows, int q_heads, int kv_heads, int head_dim,
                                                  int max_seq_len, int block_size) {
-    (void)block_size;
-    if (rows < 0 || pkv::check_heads(q_heads, kv_heads, head_dim) != PKV_OK || max_seq_len < 0)
+    if (rows < 0 || pkv::check_heads(q_heads, kv_heads, head_dim) != PKV_OK || max_seq_len < 0 ||
+        block_size <= 0)
         return 0;
+    if (pkv::tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size))
+        return pkv::tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len);
     return pkv::workspace_layout(rows, q_heads, pkv::splits_for(max_seq_len)).total;
 }
 
@@ -294,6 +299,13 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_po
     if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID_ARG;
+    if (tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size)) {
+        if (!workspace || workspace_bytes < tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len))
+            return PKV_ERR_WORKSPACE;
+        return tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads,
+                                 kv_heads, block_size, scale, max_blocks_per_row, num_blocks,
+                                 max_seq_len, 0, workspace, dev_err, stream);
+    }
     const int nsplit = splits_for(max_seq_len);
     if (!workspace || workspace_bytes < workspace_layout(rows, q_heads, nsplit).total)
         return PKV_ERR_WORKSPACE;
@@ -319,6 +331,14 @@ extern "C" int paged_attention_padded_decode(void* out, const void* q, const voi
     if (!out || !q || !seq_lens || (width > 0 && (!k_slab || !v_slab))) return PKV_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_slab) || !aligned16(v_slab))
         return PKV_ERR_INVALID_ARG;
+    // The staged kernel when the workspace is sized for it (block size 16),
+    // else the split kernel.
+    if (width > 0 && tma_decode_supported(rows, q_heads, kv_heads, head_dim, 16) && workspace &&
+        workspace_bytes >= tma_workspace_bytes(rows, q_heads, kv_heads, width)) {
+        return tma_decode_launch(out, q, k_slab, v_slab, nullptr, seq_lens, rows, q_heads,
+                                 kv_heads, 16, scale, 1, 1, width, width, workspace, dev_err,
+                                 stream);
+    }
     const int nsplit = splits_for(width);
     if (!workspace || workspace_bytes < workspace_layout(rows, q_heads, nsplit).total)
         return PKV_ERR_WORKSPACE;

@@ -69,8 +69,9 @@ extern "C" int paged_attention_decode_noalloc(void* out, const void* q, const vo
     if (st != PKV_OK) return st;
     // The array keeps the previous call's contents; the arrival counters must
     // start at zero, the partial results are written before they are read.
-    if (cudaMemsetAsync(scratch, 0, pkv::decode_workspace_zero_bytes(rows), stream) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    const size_t zero = pkv::decode_workspace_zero_bytes(rows, q_heads, kv_heads, head_dim,
+                                                         max_seq_len, block_size);
+    if (cudaMemsetAsync(scratch, 0, zero, stream) != cudaSuccess) return PKV_ERR_CUDA;
     return paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads,
                                   kv_heads, head_dim, block_size, scale, max_blocks_per_row,
                                   num_blocks, max_seq_len, scratch, kScratchBytes, dev_err, stream);

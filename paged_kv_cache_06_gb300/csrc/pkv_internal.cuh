@@ -37,6 +37,17 @@ inline int launch_status() {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Bytes at the start of a decode workspace that must be zero before a call.
-size_t decode_workspace_zero_bytes(int rows);
+size_t decode_workspace_zero_bytes(int rows, int q_heads, int kv_heads, int head_dim,
+                                   int max_seq_len, int block_size);
+
+// TMA / tensor-core decode kernel (decode_tma.cu).
+bool tma_decode_supported(int rows, int q_heads, int kv_heads, int head_dim, int block_size);
+size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len);
+size_t tma_workspace_zero_bytes(int rows, int kv_heads, int max_seq_len);
+int tma_decode_launch(void* out, const void* q, const void* k_base, const void* v_base,
+                      const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,
+                      int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
+                      int max_seq_len, int width, void* workspace, int32_t* dev_err,
+                      cudaStream_t stream);
 
 }  // namespace pkv

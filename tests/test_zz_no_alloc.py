@@ -74,10 +74,11 @@ def test_noalloc_after_a_different_shape(cuda_device):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_device):
-    rows, bs = 256, 16
-    msl = 1024
-    while ops.workspace_size(rows, 12, 2, 128, msl, bs) <= NOALLOC_BYTES:
-        msl *= 2
+    bs, msl = 16, 4096
+    for rows in (256, 512, 1024, 2048, 4096, 8192):
+        if ops.workspace_size(rows, 12, 2, 128, msl, bs) > NOALLOC_BYTES:
+            break
+    assert ops.workspace_size(rows, 12, 2, 128, msl, bs) > NOALLOC_BYTES
     mbpr = msl // bs
     q = torch.zeros(rows, 12, 128, dtype=torch.float16, device="cuda")
     pool = torch.zeros(1, bs, 2, 128, dtype=torch.float16, device="cuda")
