@@ -148,6 +148,45 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
                            void* workspace, size_t workspace_bytes, int32_t* dev_err,
                            cudaStream_t stream);
 
+/* Flags of paged_attention_append_decode. */
+#define PKV_FLAG_PDL 0x1u /* overlap this launch's start with the preceding kernel (see below) */
+
+/*
+ * paged_attention_append_decode -- one decode step of one layer: exactly
+ * paged_kv_append(k_pool, v_pool, block_tables, positions, k_new, v_new, ...)
+ * followed by paged_attention_decode(out, q, k_pool, v_pool, block_tables,
+ * seq_lens, ...), with the same arguments, results and errors as those two
+ * calls (the pools end bit-identical; the new token takes part in the
+ * attention when positions[r] < seq_lens[r]).  Defining passages: as for the
+ * two calls ("SLM paged attention", "The architecture": the new token goes to
+ * slot position % block_size of block position / block_size; decode reads
+ * every row at its true length).
+ *
+ * Where the decode kernel supports the shape (head_dim 128, group <= 8,
+ * block_size a multiple of 16, rows <= 1024) this is ONE launch: the block
+ * that stages the new token's granule takes it from k_new / v_new directly,
+ * and the pool slot is written in the same kernel.  Otherwise the two calls
+ * are made in sequence.
+ *
+ * flags: 0 or PKV_FLAG_PDL.  With PKV_FLAG_PDL the launch uses programmatic
+ * stream serialization: its blocks may start while the preceding kernel in
+ * `stream` is still running, and before that kernel completes they read
+ * seq_lens, block_tables and the cached tokens of k_pool / v_pool.  q,
+ * positions, k_new, v_new, out, the workspace and the appended slots are
+ * touched only after it completes.  The caller guarantees that the preceding
+ * kernel writes neither seq_lens, block_tables nor these pools (for example
+ * the previous layer's call, or a projection kernel).  Without the flag the
+ * launch is ordered after all earlier work as usual.
+ */
+int paged_attention_append_decode(void* out, const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* block_tables, const int32_t* seq_lens,
+                                  const int32_t* positions, const void* k_new, const void* v_new,
+                                  int rows, int q_heads, int kv_heads, int head_dim,
+                                  int block_size, float scale, int max_blocks_per_row,
+                                  int num_blocks, int max_seq_len, void* workspace,
+                                  size_t workspace_bytes, unsigned flags, int32_t* dev_err,
+                                  cudaStream_t stream);
+
 /*
  * paged_attention_padded_decode -- the comparator the paged cache replaced:
  * attention over a contiguous slab with one full-width slot per row, computed

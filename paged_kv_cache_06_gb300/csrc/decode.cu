@@ -302,9 +302,10 @@ extern "C" int paged_attention_decode(void* out, const void* q, const void* k_po
     if (tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size)) {
         if (!workspace || workspace_bytes < tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len))
             return PKV_ERR_WORKSPACE;
-        return tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads,
-                                 kv_heads, block_size, scale, max_blocks_per_row, num_blocks,
-                                 max_seq_len, 0, workspace, dev_err, stream);
+        const int st = tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows,
+                                         q_heads, kv_heads, block_size, scale, max_blocks_per_row,
+                                         num_blocks, max_seq_len, 0, workspace, dev_err, stream);
+        if (st != PKV_ERR_UNSUPPORTED) return st;
     }
     const int nsplit = splits_for(max_seq_len);
     if (!workspace || workspace_bytes < workspace_layout(rows, q_heads, nsplit).total)
@@ -347,4 +348,45 @@ extern "C" int paged_attention_padded_decode(void* out, const void* q, const voi
                                        dev_err);
     decode_split_kernel<false><<<dim3(nsplit, rows), kThreads, 0, stream>>>(p);
     return launch_status();
+}
+
+extern "C" int paged_attention_append_decode(
+    void* out, const void* q, void* k_pool, void* v_pool, const int32_t* block_tables,
+    const int32_t* seq_lens, const int32_t* positions, const void* k_new, const void* v_new, int rows,
+    int q_heads, int kv_heads, int head_dim, int block_size, float scale, int max_blocks_per_row,
+    int num_blocks, int max_seq_len, void* workspace, size_t workspace_bytes, unsigned flags,
+    int32_t* dev_err, cudaStream_t stream) {
+    using namespace pkv;
+    const int hs = check_heads(q_heads, kv_heads, head_dim);
+    if (hs != PKV_OK) return hs;
+    if (rows < 0 || block_size <= 0 || block_size > 1024 || max_blocks_per_row <= 0 ||
+        num_blocks <= 0 || max_seq_len < 0 || !isfinite(scale) || (flags & ~PKV_FLAG_PDL))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_row * block_size) return PKV_ERR_INVALID_ARG;
+    if (rows == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !positions || !k_new ||
+        !v_new)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return PKV_ERR_INVALID_ARG;
+    if (tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size)) {
+        if (!workspace || workspace_bytes < tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len))
+            return PKV_ERR_WORKSPACE;
+        const AppendArgs app{positions, k_new, v_new};
+        const int st = tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows,
+                                         q_heads, kv_heads, block_size, scale, max_blocks_per_row,
+                                         num_blocks, max_seq_len, 0, workspace, dev_err, stream,
+                                         &app, (flags & PKV_FLAG_PDL) != 0);
+        if (st != PKV_ERR_UNSUPPORTED) return st;
+    }
+    // Shapes the staged kernel does not take: the two calls in sequence.
+    const int st = paged_kv_append(k_pool, v_pool, block_tables, positions, k_new, v_new, rows,
+                                   kv_heads, head_dim, block_size, max_blocks_per_row, num_blocks,
+                                   dev_err, stream);
+    if (st != PKV_OK) return st;
+    return paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads,
+                                  kv_heads, head_dim, block_size, scale, max_blocks_per_row,
+                                  num_blocks, max_seq_len, workspace, workspace_bytes, dev_err,
+                                  stream);
 }

@@ -44,10 +44,17 @@ size_t decode_workspace_zero_bytes(int rows, int q_heads, int kv_heads, int head
 bool tma_decode_supported(int rows, int q_heads, int kv_heads, int head_dim, int block_size);
 size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len);
 size_t tma_workspace_zero_bytes(int rows, int kv_heads, int max_seq_len);
+// New-token append fused into the decode launch (positions / k_new / v_new as
+// in paged_kv_append).
+struct AppendArgs {
+    const int32_t* positions;
+    const void* k_new;
+    const void* v_new;
+};
 int tma_decode_launch(void* out, const void* q, const void* k_base, const void* v_base,
                       const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
                       int max_seq_len, int width, void* workspace, int32_t* dev_err,
-                      cudaStream_t stream);
+                      cudaStream_t stream, const AppendArgs* append = nullptr, bool pdl = false);
 
 }  // namespace pkv

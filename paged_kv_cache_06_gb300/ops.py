@@ -69,6 +69,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.pkv_check_error.restype = I
     L.paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P, P]
     L.paged_attention_decode_noalloc.restype = I
+    L.paged_attention_append_decode.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I,
+                                                P, S, ctypes.c_uint, P, P]
+    L.paged_attention_append_decode.restype = I
 
 
 def status_string(status: int) -> str:
@@ -156,6 +159,34 @@ def decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale: float, max_seq
                                       _ptr(workspace), workspace.numel(), _ptr(dev_err),
                                       _stream(stream))
     _check("paged_attention_decode", st)
+
+
+PKV_FLAG_PDL = 0x1
+
+
+def append_decode(out, q, k_pool, v_pool, block_tables, seq_lens, positions, k_new, v_new,
+                  scale: float, max_seq_len: int, workspace, pdl: bool = False, dev_err=None,
+                  stream=None):
+    """paged_attention_append_decode: append each row's new token, then decode
+    (one fused launch where supported; ``pdl`` overlaps it with the previous
+    kernel under the contract stated in include/paged_kv.h)."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1),
+                         (positions, "positions", torch.int32, 1),
+                         (k_new, "k_new", torch.float16, 3), (v_new, "v_new", torch.float16, 3),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_append_decode(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(positions), _ptr(k_new), _ptr(v_new), rows, hq, hk, d, bs, float(scale),
+        block_tables.shape[1], nb, int(max_seq_len), _ptr(workspace), workspace.numel(),
+        PKV_FLAG_PDL if pdl else 0, _ptr(dev_err), _stream(stream))
+    _check("paged_attention_append_decode", st)
 
 
 def padded_decode(out, q, k_slab, v_slab, seq_lens, scale: float, workspace, dev_err=None,

@@ -265,3 +265,91 @@ def test_cuda_graph_of_layers_matches_eager(cuda_device):
     rows = [int(np.argmax(case.seq_lens)), 3]
     _, _, ref = oracle_after_append(case, 2, rows=rows)
     assert_close(outs[2][rows], ref, "graph layer 2")
+
+
+# --- fused append + decode ---------------------------------------------------
+
+def _fused_vs_separate(case, pdl=False):
+    d1 = wl.to_device(case)
+    d2 = wl.to_device(case)
+    ws1 = ops.alloc_workspace(case.rows, case.q_heads, case.kv_heads, case.head_dim,
+                              case.max_seq_len, case.block_size)
+    ws2 = ops.alloc_workspace(case.rows, case.q_heads, case.kv_heads, case.head_dim,
+                              case.max_seq_len, case.block_size)
+    o1 = torch.full((case.rows, case.q_heads, case.head_dim), float("nan"), dtype=torch.float16,
+                    device="cuda")
+    o2 = torch.full_like(o1, float("nan"))
+    ops.append(d1["k_pool"][0], d1["v_pool"][0], d1["block_tables"], d1["positions"],
+               d1["k_new"][0], d1["v_new"][0])
+    ops.decode(o1, d1["q"][0], d1["k_pool"][0], d1["v_pool"][0], d1["block_tables"],
+               d1["seq_lens"], case.scale, case.max_seq_len, ws1)
+    ops.append_decode(o2, d2["q"][0], d2["k_pool"][0], d2["v_pool"][0], d2["block_tables"],
+                      d2["seq_lens"], d2["positions"], d2["k_new"][0], d2["v_new"][0], case.scale,
+                      case.max_seq_len, ws2, pdl=pdl)
+    torch.cuda.synchronize()
+    return o1, o2, d1, d2
+
+
+@pytest.mark.parametrize("lengths,bs", [([1, 17, 64, 200], 16), ([5, 64, 65, 1, 4096, 300], 64),
+                                        ([700, 33, 64, 65], 32), ([77, 300], 7)])
+def test_append_decode_equals_append_then_decode(cuda_device, lengths, bs):
+    case = wl.custom(lengths, bs, seed=11, nan_fill=True, extra_blocks=2)
+    o1, o2, d1, d2 = _fused_vs_separate(case)
+    assert torch.equal(d1["k_pool"].view(torch.int16), d2["k_pool"].view(torch.int16))
+    assert torch.equal(d1["v_pool"].view(torch.int16), d2["v_pool"].view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    _, _, ref = oracle_after_append(case, 0)
+    assert_close(o2, ref, "fused append+decode")
+
+
+def test_append_decode_position_before_the_end_and_past_it(cuda_device):
+    # positions < seq_len - 1 overwrite an older slot that is attended to;
+    # positions >= seq_len are written but not attended to.
+    case = wl.custom([40, 100, 33], 16, seed=12, nan_fill=False, append=False)
+    case.positions[:] = [10, 100, 50]
+    case.block_tables[1, 6] = case.num_blocks - 1 if case.block_tables[1, 6] < 0 else case.block_tables[1, 6]
+    o1, o2, d1, d2 = _fused_vs_separate(case)
+    assert torch.equal(d1["k_pool"].view(torch.int16), d2["k_pool"].view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_append_decode_pdl_graph_of_layers_matches_eager(cuda_device):
+    case = wl.mixed(layers=4)
+    d = wl.to_device(case)
+    ws = ops.alloc_workspace(case.rows, 12, 2, 128, case.max_seq_len, 64)
+    outs = torch.zeros(case.layers, case.rows, 12, 128, dtype=torch.float16, device="cuda")
+
+    def step(pdl):
+        for l in range(case.layers):
+            ops.append_decode(outs[l], d["q"][l], d["k_pool"][l], d["v_pool"][l],
+                              d["block_tables"], d["seq_lens"], d["positions"], d["k_new"][l],
+                              d["v_new"][l], case.scale, case.max_seq_len, ws, pdl=pdl)
+
+    step(False)
+    torch.cuda.synchronize()
+    eager = outs.clone()
+    outs.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(True)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), outs.view(torch.int16))
+    rows = [int(np.argmax(case.seq_lens)), 5]
+    _, _, ref = oracle_after_append(case, 3, rows=rows)
+    assert_close(outs[3][rows], ref, "pdl graph layer 3")
+
+
+def test_many_rows_use_the_split_kernel(cuda_device):
+    # more rows than the staged kernel takes: the split kernel serves them
+    lengths = (np.arange(1100) % 37 + 1).tolist()
+    case = wl.custom(lengths, 16, seed=13, nan_fill=True)
+    out, *_ = run_gpu(case)
+    rows = [0, 36, 555, 1099]
+    _, _, ref = oracle_after_append(case, 0, rows=rows)
+    assert_close(out[rows], ref, "1100 rows")
