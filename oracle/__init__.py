@@ -81,6 +81,10 @@ def _load():
             lib.oracle_blockwise_decode.restype = I
             lib.oracle_paged_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I]
             lib.oracle_paged_append.restype = I
+            lib.oracle_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I]
+            lib.oracle_copy_blocks.restype = I
+            lib.oracle_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I]
+            lib.oracle_prefill_scatter.restype = I
             _lib = lib
     return _lib
 
@@ -184,4 +188,28 @@ def paged_append(k_pool, v_pool, block_tables, positions, k_new, v_new):
     rc = _load().oracle_paged_append(_ptr(kp), _ptr(vp), _ptr(bt), _ptr(pos), _ptr(kn), _ptr(vn),
                                      rows, hk, d, bs, bt.shape[1] if bt.ndim == 2 else 0, nb)
     _check(rc, "paged_append")
+    return kp, vp
+
+
+def copy_blocks(k_pool, v_pool, src_ids, dst_ids):
+    """Return copies of the pools with block dst_ids[i] := block src_ids[i] (in order)."""
+    kp = _bits(k_pool).copy(); vp = _bits(v_pool).copy()
+    src = _i32(src_ids); dst = _i32(dst_ids)
+    nb, bs, hk, d = kp.shape
+    rc = _load().oracle_copy_blocks(_ptr(kp), _ptr(vp), _ptr(src), _ptr(dst), int(src.shape[0]),
+                                    bs, hk, d, nb)
+    _check(rc, "copy_blocks")
+    return kp, vp
+
+
+def prefill_scatter(k_pool, v_pool, block_tables, src_start, dst_start, lengths, k_src, v_src):
+    """Return copies of the pools with each row's prompt tokens laid into its blocks."""
+    kp = _bits(k_pool).copy(); vp = _bits(v_pool).copy()
+    bt = _i32(block_tables); ss = _i32(src_start); ds = _i32(dst_start); ln = _i32(lengths)
+    ks = _bits(k_src); vs = _bits(v_src)
+    nb, bs, hk, d = kp.shape
+    rows, width = ks.shape[0], ks.shape[1]
+    rc = _load().oracle_prefill_scatter(_ptr(kp), _ptr(vp), _ptr(bt), _ptr(ss), _ptr(ds), _ptr(ln),
+                                        _ptr(ks), _ptr(vs), rows, width, hk, d, bs, bt.shape[1], nb)
+    _check(rc, "prefill_scatter")
     return kp, vp

@@ -345,3 +345,69 @@ int oracle_paged_append(uint16_t* k_pool, uint16_t* v_pool, const int32_t* block
     }
     return ORACLE_OK;
 }
+
+/*
+ * Copy-on-write block copy: for i < n, block dst_ids[i] of both pools becomes
+ * a byte copy of block src_ids[i] ("SLM paged attention", section "The
+ * architecture": the manager clones just the shared block a writer must
+ * write into and repoints the writer's table entry).  In place; pairs are
+ * applied in order.  Ids outside [0, num_blocks) are an error.
+ */
+int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* src_ids,
+                       const int32_t* dst_ids, int n, int block_size, int kv_heads,
+                       int head_dim, int num_blocks) {
+    if (n < 0 || block_size <= 0 || kv_heads <= 0 || head_dim <= 0) return ORACLE_BAD_ARG;
+    for (int i = 0; i < n; ++i)
+        if (src_ids[i] < 0 || src_ids[i] >= num_blocks || dst_ids[i] < 0 || dst_ids[i] >= num_blocks)
+            return ORACLE_BAD_TABLE;
+    const int64_t per_block = (int64_t)block_size * kv_heads * head_dim;
+    for (int i = 0; i < n; ++i) {
+        memmove(k_pool + dst_ids[i] * per_block, k_pool + src_ids[i] * per_block,
+                sizeof(uint16_t) * (size_t)per_block);
+        memmove(v_pool + dst_ids[i] * per_block, v_pool + src_ids[i] * per_block,
+                sizeof(uint16_t) * (size_t)per_block);
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Prefill scatter: after a batched prefill whose rows were left-padded to the
+ * group's widest prompt, each row's K/V is copied into its blocks with the
+ * padding dropped ("Paged attention", section "What changed").  Source
+ * k_src, v_src: [rows][width][kv_heads][head_dim]; row r's tokens are columns
+ * src_start[r] .. src_start[r] + lengths[r] - 1 and go to logical positions
+ * dst_start[r] .. dst_start[r] + lengths[r] - 1 of the row's table.  Rows
+ * with lengths[r] <= 0 are skipped.  A position whose logical block is past
+ * the table or whose id is out of range is an error.
+ */
+int oracle_prefill_scatter(uint16_t* k_pool, uint16_t* v_pool, const int32_t* block_tables,
+                           const int32_t* src_start, const int32_t* dst_start,
+                           const int32_t* lengths, const uint16_t* k_src, const uint16_t* v_src,
+                           int rows, int width, int kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_row, int num_blocks) {
+    if (rows < 0 || width < 0 || kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return ORACLE_BAD_ARG;
+    const int64_t tok = (int64_t)kv_heads * head_dim;
+    for (int r = 0; r < rows; ++r) {
+        if (lengths[r] <= 0) continue;
+        if (src_start[r] < 0 || src_start[r] + lengths[r] > width || dst_start[r] < 0)
+            return ORACLE_BAD_ARG;
+        for (int t = 0; t < lengths[r]; ++t) {
+            const int pos = dst_start[r] + t;
+            if (pos / block_size >= max_blocks_per_row) return ORACLE_BAD_TABLE;
+            const int32_t pb = block_tables[(int64_t)r * max_blocks_per_row + pos / block_size];
+            if (pb < 0 || pb >= num_blocks) return ORACLE_BAD_TABLE;
+        }
+    }
+    for (int r = 0; r < rows; ++r) {
+        for (int t = 0; t < lengths[r]; ++t) {
+            const int pos = dst_start[r] + t;
+            const int32_t pb = block_tables[(int64_t)r * max_blocks_per_row + pos / block_size];
+            const int64_t dst = ((int64_t)pb * block_size + pos % block_size) * tok;
+            const int64_t src = ((int64_t)r * width + src_start[r] + t) * tok;
+            memcpy(k_pool + dst, k_src + src, sizeof(uint16_t) * (size_t)tok);
+            memcpy(v_pool + dst, v_src + src, sizeof(uint16_t) * (size_t)tok);
+        }
+    }
+    return ORACLE_OK;
+}

@@ -269,3 +269,76 @@ def test_append_position_beyond_table_is_an_error():
     with pytest.raises(oracle.OracleError):
         oracle.paged_append(c.k_pool[0], c.v_pool[0], c.block_tables, np.array([4], np.int32),
                             c.k_new[0], c.v_new[0])
+
+
+# --- copy-on-write block copy and prefill scatter -----------------------------
+
+def test_golden_copy_on_write_pairs_in_order():
+    g = json.load(open(os.path.join(GOLDEN, "cow_prefill_hand.json")))
+    nb, bs, hk, d = g["num_blocks"], g["block_size"], g["kv_heads"], g["head_dim"]
+    base = np.arange(nb * bs * hk * d, dtype=np.float32).reshape(nb, bs, hk, d)
+    kp, vp = _f16(base), _f16(-base)
+    k2, v2 = oracle.copy_blocks(kp, vp, g["cow"]["src"], g["cow"]["dst"])
+    ek, ev = kp.copy(), vp.copy()
+    for s, t in zip(g["cow"]["src"], g["cow"]["dst"]):
+        ek[t] = ek[s]
+        ev[t] = ev[s]
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+    assert np.array_equal(k2[[1, 2, 4, 5]], kp[[1, 2, 4, 5]])
+
+
+def test_copy_on_write_then_repoint_keeps_decode_exact():
+    # cloning a shared block and repointing one row at the clone changes nothing
+    c = wl.custom([20, 20], 8, seed=30, append=False, nan_fill=True, extra_blocks=4,
+                  shared_tokens=16)
+    shared = c.block_tables[1, 1]
+    spare = c.num_blocks - 1
+    kp, vp = oracle.copy_blocks(c.k_pool[0], c.v_pool[0], [shared], [spare])
+    bt = c.block_tables.copy()
+    bt[1, 1] = spare
+    a = oracle.paged_decode(c.q[0], c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    b = oracle.paged_decode(c.q[0], kp, vp, bt, c.seq_lens, c.scale)
+    assert np.array_equal(a, b)
+
+
+def test_copy_blocks_rejects_bad_ids():
+    c = wl.custom([4], 4, seed=31, nan_fill=True)
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(c.k_pool[0], c.v_pool[0], [0], [c.num_blocks])
+
+
+def test_golden_prefill_scatter_drops_left_padding():
+    g = json.load(open(os.path.join(GOLDEN, "cow_prefill_hand.json")))
+    pf = g["prefill"]
+    nb, bs, hk, d = g["num_blocks"], g["block_size"], g["kv_heads"], g["head_dim"]
+    kp = np.full((nb, bs, hk, d), wl.FP16_NAN_BITS, np.uint16)
+    ks = _f16(pf["k_src"])
+    bt = np.array(pf["block_tables"], np.int32)
+    # row 1 targets a -1 entry: an error, nothing written
+    with pytest.raises(oracle.OracleError):
+        oracle.prefill_scatter(kp, kp, bt, pf["src_start"], pf["dst_start"], pf["lengths"], ks, ks)
+    lengths = [pf["lengths"][0], 0]
+    k2, _ = oracle.prefill_scatter(kp, kp, bt, pf["src_start"], pf["dst_start"], lengths, ks, ks)
+    ek = kp.copy()
+    for w in pf["expected_writes_row0"]:
+        ek[w["block"], w["slot"], 0] = _f16(w["k"])
+    assert np.array_equal(k2, ek)
+
+
+def test_prefill_scatter_then_gather_recovers_the_prompts():
+    c = wl.custom([37, 5, 64, 1], 16, seed=32, append=False, nan_fill=True)
+    rng = np.random.default_rng(3)
+    width = 70
+    ks = rng.standard_normal((c.rows, width, c.kv_heads, c.head_dim)).astype(np.float16)
+    vs = rng.standard_normal((c.rows, width, c.kv_heads, c.head_dim)).astype(np.float16)
+    lengths = c.seq_lens.copy()
+    src_start = (width - lengths).astype(np.int32)      # left padded
+    dst_start = np.zeros(c.rows, np.int32)
+    kp, vp = oracle.prefill_scatter(c.k_pool[0], c.v_pool[0], c.block_tables, src_start, dst_start,
+                                    lengths, ks, vs)
+    import dataclasses
+    c2 = dataclasses.replace(c, k_pool=kp[None], v_pool=vp[None])
+    for r in range(c.rows):
+        k, v = wl.logical_tokens(c2, 0, r)
+        assert np.array_equal(k, ks[r, src_start[r]:].view(np.uint16))
+        assert np.array_equal(v, vs[r, src_start[r]:].view(np.uint16))
