@@ -102,6 +102,44 @@ int paged_kv_append(void* k_pool, void* v_pool, const int32_t* block_tables,
                     cudaStream_t stream);
 
 /*
+ * paged_kv_copy_blocks -- copy-on-write: for i < n, block dst_ids[i] of both
+ * pools becomes a bit-exact copy of block src_ids[i].  Defining passage:
+ * "SLM paged attention", sections "The architecture" and "End-to-end flow"
+ * (a writer about to write into a shared block gets a clone of just that
+ * block; its table entry is then repointed).  The pairs come from
+ * pkv_bm_append_slot.  The dst ids must be distinct and must not appear among
+ * the src ids of the same call (pairs run concurrently).  An id outside
+ * [0, num_blocks) skips its pair and sets PKV_DEV_ERR_BLOCK_ID.
+ * src_ids, dst_ids: device int32 [n].  head_dim must be a multiple of 8.
+ */
+int paged_kv_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_ids,
+                         const int32_t* dst_ids, int n, int block_size, int kv_heads,
+                         int head_dim, int num_blocks, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * paged_kv_prefill_scatter -- lay a batched prefill's K/V into the rows'
+ * blocks with the padding dropped.  Defining passage: "Paged attention",
+ * section "What changed" (newly admitted requests are prefilled together,
+ * left padded to the group's widest prompt, after which each row's KV is
+ * copied into its blocks with the padding dropped).
+ *
+ * k_src, v_src: fp16 [rows][width][kv_heads][head_dim].  For each row r with
+ * lengths[r] > 0, source columns src_start[r] .. src_start[r] + lengths[r] - 1
+ * go to logical positions dst_start[r] .. of the row (slot pos % block_size
+ * of block block_tables[r][pos / block_size]); left padding is
+ * src_start[r] = width - lengths[r].  A source range past the width sets
+ * PKV_DEV_ERR_POSITION and skips the row; a position past the table or an id
+ * out of range skips that token and sets PKV_DEV_ERR_POSITION /
+ * PKV_DEV_ERR_BLOCK_ID.  Bit-exact copy.
+ */
+int paged_kv_prefill_scatter(void* k_pool, void* v_pool, const int32_t* block_tables,
+                             const int32_t* src_start, const int32_t* dst_start,
+                             const int32_t* lengths, const void* k_src, const void* v_src,
+                             int rows, int width, int kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_row, int num_blocks, int32_t* dev_err,
+                             cudaStream_t stream);
+
+/*
  * paged_attention_workspace_size -- bytes of device workspace that
  * paged_attention_decode needs for these sizes (the split-K partial results
  * and per-row arrival counters).  Pure host arithmetic; never fails (returns

@@ -72,6 +72,10 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_append_decode.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I,
                                                 P, S, ctypes.c_uint, P, P]
     L.paged_attention_append_decode.restype = I
+    L.paged_kv_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
+    L.paged_kv_copy_blocks.restype = I
+    L.paged_kv_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
+    L.paged_kv_prefill_scatter.restype = I
 
 
 def status_string(status: int) -> str:
@@ -125,6 +129,40 @@ def append(k_pool, v_pool, block_tables, positions, k_new, v_new, dev_err=None, 
                                _ptr(k_new), _ptr(v_new), rows, hk, d, bs, block_tables.shape[1], nb,
                                _ptr(dev_err), _stream(stream))
     _check("paged_kv_append", st)
+
+
+def copy_blocks(k_pool, v_pool, src_ids, dst_ids, dev_err=None, stream=None):
+    """paged_kv_copy_blocks: block dst_ids[i] := block src_ids[i] in both pools."""
+    for t, n, dt, nd in ((k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (src_ids, "src_ids", torch.int32, 1), (dst_ids, "dst_ids", torch.int32, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    if src_ids.shape != dst_ids.shape:
+        raise ValueError("src_ids and dst_ids must have the same length")
+    nb, bs, hk, d = k_pool.shape
+    st = lib().paged_kv_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(src_ids), _ptr(dst_ids),
+                                    src_ids.shape[0], bs, hk, d, nb, _ptr(dev_err), _stream(stream))
+    _check("paged_kv_copy_blocks", st)
+
+
+def prefill_scatter(k_pool, v_pool, block_tables, src_start, dst_start, lengths, k_src, v_src,
+                    dev_err=None, stream=None):
+    """paged_kv_prefill_scatter: copy each row's prompt K/V into its blocks."""
+    for t, n, dt, nd in ((k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (src_start, "src_start", torch.int32, 1),
+                         (dst_start, "dst_start", torch.int32, 1),
+                         (lengths, "lengths", torch.int32, 1),
+                         (k_src, "k_src", torch.float16, 4), (v_src, "v_src", torch.float16, 4)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    nb, bs, hk, d = k_pool.shape
+    rows, width = k_src.shape[0], k_src.shape[1]
+    st = lib().paged_kv_prefill_scatter(_ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                        _ptr(src_start), _ptr(dst_start), _ptr(lengths), _ptr(k_src),
+                                        _ptr(v_src), rows, width, hk, d, bs, block_tables.shape[1],
+                                        nb, _ptr(dev_err), _stream(stream))
+    _check("paged_kv_prefill_scatter", st)
 
 
 def workspace_size(rows: int, q_heads: int, kv_heads: int, head_dim: int, max_seq_len: int,
