@@ -14,20 +14,31 @@
 // SM), so every SM moves the same number of bytes whatever the length mix.
 // Each block derives the partition itself from seq_lens (a block-wide scan),
 // so the host never reads device lengths.  The part of a unit inside one
-// block is a piece; a unit with several pieces is merged by a fan-in-8 tree
-// of last-arriving blocks (per-node atomic counters, re-armed by the merger).
+// block is a piece.  A unit with pieces in several blocks is merged by the
+// block that holds its last piece: every piece publishes a partial record
+// (running max, sum and unnormalised output) and counts itself on a per-unit
+// counter with a release; the merging block waits (bounded) until the others
+// have all counted, lands every record and combines them through their
+// log-sum-exp, then re-arms the counter.  A block merges at most one unit.
 //
 // Block layout.  Warp 4 is the producer: it resolves each granule's physical
 // block from the table and issues TMA tiled copies (a 16-token x 64-dim box,
-// 128-byte swizzle, never crossing a physical block) into a 3-stage mbarrier
-// pipeline; the first tile of a piece also brings the unit's query heads by
-// a bulk copy.  Warps 0-3 consume one granule each per stage:
+// 128-byte swizzle, never crossing a physical block) into a ring of twelve
+// 8 KB granule slots.  Warps 0-3 consume, in one of two modes:
+//   * burst: the block's whole range fits the ring and covers at most four
+//     pieces.  Every copy is issued before the dependency wait, warps are
+//     dealt to pieces in proportion to their size, and each warp attends to
+//     its granules (up to three at once) in one pass; the warps' partial
+//     states are then combined for all pieces together.
+//   * stream: the ring runs as three stages of four granules, one granule
+//     per warp per stage, and pieces are combined as they end.
+// Per granule (16 tokens) and group of query heads (up to 8):
 //   S^T[16 tok][8 heads] = K[16 tok][128] . Q^T        (mma.sync m16n8k16)
 //   online softmax per head in fp32, base-2 exponent
 //   O^T[128][8 heads]   += V^T[128][16 tok] . P^T      (P transposed in
 //                                                       registers by movmatrix)
-// The grouped query heads (up to 8) are the MMA's N = 8 columns, so every K
-// and V byte is read once and feeds all heads of its group.
+// The grouped query heads are the MMA's N = 8 columns, so every K and V byte
+// is read once and feeds all heads of its group.
 //
 // Safety: table entries are range-checked before any copy is issued (a bad
 // entry is skipped and flagged); every mbarrier wait is bounded and a timeout
@@ -43,8 +54,9 @@ namespace pkv {
 namespace tma {
 
 constexpr int kGranule = 16;        // tokens per box and per consumer warp step
-constexpr int kTileGranules = 4;    // granules per pipeline stage (64 tokens)
+constexpr int kTileGranules = 4;    // stream mode: granules per stage (one per consumer warp)
 constexpr int kStages = 3;
+constexpr int kRing = kStages * kTileGranules;  // granule slots
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
@@ -53,18 +65,21 @@ constexpr int kMaxRows = 1024;
 constexpr int kRecHead = 16;   // per record: m[8], l[8], then o[group][128]
 constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
 constexpr int kMergeBatch = 8; // children merged per register batch
-constexpr uint32_t kBoxBytes = kGranule * 128;                // 16 rows x 128 B
-constexpr uint32_t kHalfBytes = kTileGranules * kBoxBytes;    // one 64-dim half of 64 tokens
-constexpr uint32_t kStageK = 0;
-constexpr uint32_t kStageV = 2 * kHalfBytes;
-constexpr uint32_t kStageQ = 4 * kHalfBytes;
-constexpr uint32_t kStageBytes = 4 * kHalfBytes + 8 * 256;    // K, V, Q (8 heads x 256 B)
-constexpr int kCombStride = 68;                               // 64 dims + 4 pad (floats)
+constexpr int kBurstPieces = 4;
+constexpr int kBatch = 3;      // burst mode: granules attended together by one warp
+constexpr int kCounterStride = 32;  // ints between the arrival counters of two units
+constexpr uint32_t kPollLimit = 1u << 21;  // polls of a merge wait (about a second)
+constexpr uint32_t kBoxBytes = kGranule * 128;   // 16 rows x 128 B (64 dims)
+constexpr uint32_t kSlotBytes = 4 * kBoxBytes;   // K dims 0-63, K 64-127, V 0-63, V 64-127
+constexpr uint32_t kSlotV = 2 * kBoxBytes;
+constexpr uint32_t kQBytes = 8 * 256;            // up to 8 query heads x 128 dims
+constexpr int kCombStride = 68;                  // stream combine: 64 dims + 4 pad (floats)
+constexpr int kDumpStride = 132;                 // burst dump: 128 dims + 4 pad (floats)
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
-static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
-static_assert(2 * kStages * 8 + 8 <= 64, "barrier area");
+static_assert(kSlotBytes % 1024 == 0, "slots must keep 1024-byte alignment for 128B swizzle");
+static_assert((kRecHead + 8 * kDumpStride) * 4 <= (int)kSlotBytes, "a dumped partial fits one slot");
 
 struct Params {
     __half* out;
@@ -76,7 +91,7 @@ struct Params {
     int width;      // padded comparator: columns per row (0 = paged)
     float scale_log2;
     int rec_floats; // floats per record: 16 + group * 128
-    int* counters;  // [units]: pieces arrived per split unit (zero between calls)
+    int* counters;  // [units][kCounterStride]: pieces arrived per split unit (zero between calls)
     float* records; // [slots][rec_floats]: partial results of split units
     int32_t* dev_err;
     // fused append (all null when the kernel only decodes)
@@ -87,20 +102,34 @@ struct Params {
     __half* vpool;
 };
 
+// Burst-mode plan of one block, written by thread 0 after the prologue.
+struct Plan {
+    int burst, npieces;
+    int r[kBurstPieces], kvh[kBurstPieces], ustart[kBurstPieces], n[kBurstPieces];
+    int P[kBurstPieces], cstart[kBurstPieces], w0[kBurstPieces], wn[kBurstPieces];
+    int wpiece[kConsumerWarps], wa[kConsumerWarps], wb[kConsumerWarps];
+    int valid[kRing];
+};
+
 // Shared memory carve-up (offsets from a 1024-aligned base).
 struct Smem {
-    static constexpr uint32_t stages = 0;
-    static constexpr uint32_t comb = kStages * kStageBytes;                         // [4][8][68] f32
+    static constexpr uint32_t ring = 0;
+    static constexpr uint32_t q = ring + kRing * kSlotBytes;                        // [stages] stream queries
+    static constexpr uint32_t comb = q + kStages * kQBytes;                         // [4][8][68] f32
     static constexpr uint32_t ml = comb + kConsumerWarps * 8 * kCombStride * 4;     // [4][8] m, [4][8] l
-    static constexpr uint32_t bars = ml + 2 * kConsumerWarps * 8 * 4;               // full[S], empty[S], merge
-    static constexpr uint32_t desc = bars + 64;                                     // TileDesc[S]
-    static constexpr uint32_t flags = desc + kStages * 64;                          // misc ints
+    static constexpr uint32_t bars = ml + 2 * kConsumerWarps * 8 * 4;               // full[S], empty[S], slot[R], merge
+    static constexpr uint32_t desc = bars + (2 * kStages + kRing + 2) * 8;          // TileDesc[S]
+    static constexpr uint32_t plan = desc + kStages * 64;
+    static constexpr uint32_t flags = plan + ((sizeof(Plan) + 15) / 16) * 16;       // misc ints
     static constexpr uint32_t ppos = flags + 16 * 4;                                // piece positions [32]
     static constexpr uint32_t part = comb;  // scan partials: prologue only, aliases comb
     static constexpr uint32_t prefix = ppos + kMaxPieces * 4;                       // rows + 1 ints
-    __host__ __device__ static uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
-    __host__ __device__ static uint32_t total(int rows) { return lens(rows) + (uint32_t)rows * 4 + 1024; }
+    __host__ __device__ static constexpr uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
+    __host__ __device__ static constexpr uint32_t total(int rows) { return lens(rows) + (uint32_t)rows * 4 + 1024; }
 };
+// Two blocks per SM (this layer's and the next one's, under programmatic
+// dependent launch) at batch 32: 228 KB per SM, 1 KB reserved per block.
+static_assert(Smem::total(32) + 1024 <= 233472 / 2, "two blocks per SM at 32 rows");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -191,7 +220,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Per-stage tile descriptor: written by the producer before the stage's
+// Stream-mode tile descriptor: written by the producer before the stage's
 // full barrier is armed, read by the consumers after it completes.
 struct TileDesc {
     int ustart;                 // unit's first granule (global index)
@@ -225,20 +254,162 @@ __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Running softmax state of one warp: per lane, heads 2tq and 2tq+1
+// (tq = lane & 3) and the O^T fragments of all eight 16-dim row groups.
+struct Soft {
+    float m0, m1, l0, l1;
+    float o[8][4];
+    __device__ __forceinline__ void reset() {
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+};
+
+// One online-softmax step of a warp over kB granules staged in slots
+// slot[0..kB-1] (K dims 0-63 at +0, K 64-127 at +2 KB, V at +4 KB / +6 KB,
+// 128-byte swizzled rows), valid[j] tokens each.  Rows past valid[j] must
+// hold finite values (zeroed by the caller) so that 0 * V stays 0.
+template <int kB>
+__device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], const uint32_t* slot,
+                                       const int* valid, float scale_log2, int lane) {
+    const int gq = lane >> 2;
+    float s[kB][4];
+    {
+        // S^T = K . Q^T; per granule two independent chains (even / odd k-steps)
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        float c0[kB][4], c1[kB][4];
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c0[j][i] = c1[j][i] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int chunk = (ks & 3) * 2 + (lane >> 4);
+            const uint32_t off = (ks >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(slot[j] + off, a0, a1, a2, a3);
+                mma16816((ks & 1) ? c1[j] : c0[j], a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[j][i] = c0[j][i] + c1[j][i];
+    }
+    // scores: s0 = (tok gq, head 2tq), s1 = (gq, 2tq+1), s2/3 = tok gq+8
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+        const int v = valid[j];
+        s[j][0] = gq < v ? s[j][0] * scale_log2 : -INFINITY;
+        s[j][1] = gq < v ? s[j][1] * scale_log2 : -INFINITY;
+        s[j][2] = gq + 8 < v ? s[j][2] * scale_log2 : -INFINITY;
+        s[j][3] = gq + 8 < v ? s[j][3] * scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
+        mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(st.m0 - mu0), al1 = fast_exp2(st.m1 - mu1);
+    st.m0 = mn0;
+    st.m1 = mn1;
+    uint32_t pb0[kB], pb1[kB];
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+        const uint32_t px = pack_half2(fast_exp2(s[j][0] - mu0), fast_exp2(s[j][1] - mu1));
+        const uint32_t py = pack_half2(fast_exp2(s[j][2] - mu0), fast_exp2(s[j][3] - mu1));
+        // the sum takes the fp16 weights the MMA multiplies by
+        const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&px));
+        const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&py));
+        ls0 += fx.x + fy.x;
+        ls1 += fx.y + fy.y;
+        // B fragments of P^T (token x head) by transposing in registers
+        pb0[j] = movmatrix_t(px);
+        pb1[j] = movmatrix_t(py);
+    }
+    st.l0 = st.l0 * al0 + ls0;
+    st.l1 = st.l1 * al1 + ls1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        st.o[i][0] *= al0;
+        st.o[i][1] *= al1;
+        st.o[i][2] *= al0;
+        st.o[i][3] *= al1;
+    }
+    // O^T += V^T . P^T
+    const int row = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
+        const uint32_t off = kSlotV + (mt >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(slot[j] + off, a0, a1, a2, a3);
+            mma16816(st.o[mt], a0, a1, a2, a3, pb0[j], pb1[j]);
+        }
+    }
+}
+
+// Prepares a staged granule for attend: zeroes V rows past `valid` (they may
+// hold anything, NaN included) and overwrites row patch_row with the new
+// token (lanes 0-15 carry its K, lanes 16-31 its V, 16 bytes each).  Returns
+// whether shared memory was written.
+__device__ __forceinline__ bool prepare_granule(unsigned char* slot_ptr, int valid, int patch_row,
+                                                const uint4& patch_val, int lane) {
+    bool wrote = false;
+    if (valid < kGranule) {
+        uint4* v0 = reinterpret_cast<uint4*>(slot_ptr + kSlotV);
+        for (int i = lane; i < (kGranule - valid) * 8; i += 32) {
+            const int row = valid + (i >> 3);
+            v0[row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
+            v0[kBoxBytes / 16 + row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
+        }
+        wrote = true;
+    }
+    if (patch_row >= 0 && patch_row < valid) {
+        const int c16 = lane & 15;  // 16-byte chunk of the 128 dims
+        unsigned char* box = slot_ptr + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
+        *reinterpret_cast<uint4*>(box + patch_row * 128 + (((c16 & 7) ^ (patch_row & 7)) << 4)) =
+            patch_val;
+        wrote = true;
+    }
+    return wrote;
+}
+
 // Log-sum-exp merge of P partial records (children j = 0..P-1, rec_floats
 // apart) for head mh, dims md..md+7: M = max_j m_j, then
 // L = sum_j 2^(m_j - M) l_j and o = sum_j 2^(m_j - M) o_j, summed in child order
 // into two accumulator sets (even / odd j) added at the end.  The arithmetic
 // is the same whether the records are read from shared or global memory, so
 // the result never depends on which block merges.
+template <bool kGlobal>
 __device__ __forceinline__ void merge_children(const float* base, int P, int rec_floats, int mh,
-                                               int md, bool global, float& Ls_out, float* acc) {
-    auto ld1 = [&](const float* a) { return global ? __ldcg(a) : *a; };
+                                               int md, float& Ls_out, float* acc) {
+    auto ld1 = [&](const float* a) { return kGlobal ? __ldcg(a) : *a; };
     auto ld4 = [&](const float* a) {
-        return global ? __ldcg(reinterpret_cast<const float4*>(a)) : *reinterpret_cast<const float4*>(a);
+        return kGlobal ? __ldcg(reinterpret_cast<const float4*>(a)) : *reinterpret_cast<const float4*>(a);
     };
     float M = -INFINITY;
-    for (int j = 0; j < P; ++j) M = fmaxf(M, ld1(base + (int64_t)j * rec_floats + mh));
+    for (int j0 = 0; j0 < P; j0 += kMergeBatch) {
+        float t[kMergeBatch];
+#pragma unroll
+        for (int c = 0; c < kMergeBatch; ++c)
+            t[c] = j0 + c < P ? ld1(base + (int64_t)(j0 + c) * rec_floats + mh) : -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kMergeBatch; ++c) M = fmaxf(M, t[c]);
+    }
     float acc2[8], Ls = 0.f, Ls2 = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = acc2[i] = 0.f;
@@ -261,19 +432,138 @@ __device__ __forceinline__ void merge_children(const float* base, int P, int rec
                 }
             }
 #pragma unroll
-            for (int c = 0; c < kMergeBatch; ++c) {
-                const float wt = fast_exp2(w[c] - M);
-                float* a = (c & 1) ? acc2 : acc;
-                float& L = (c & 1) ? Ls2 : Ls;
-                L += wt * l[c];
-                a[0] += wt * x[c].x; a[1] += wt * x[c].y; a[2] += wt * x[c].z; a[3] += wt * x[c].w;
-                a[4] += wt * y[c].x; a[5] += wt * y[c].y; a[6] += wt * y[c].z; a[7] += wt * y[c].w;
+            for (int c = 0; c < kMergeBatch; c += 2) {
+                const float wa = fast_exp2(w[c] - M), wb = fast_exp2(w[c + 1] - M);
+                Ls += wa * l[c];
+                Ls2 += wb * l[c + 1];
+                acc[0] += wa * x[c].x; acc[1] += wa * x[c].y; acc[2] += wa * x[c].z; acc[3] += wa * x[c].w;
+                acc[4] += wa * y[c].x; acc[5] += wa * y[c].y; acc[6] += wa * y[c].z; acc[7] += wa * y[c].w;
+                acc2[0] += wb * x[c + 1].x; acc2[1] += wb * x[c + 1].y; acc2[2] += wb * x[c + 1].z;
+                acc2[3] += wb * x[c + 1].w; acc2[4] += wb * y[c + 1].x; acc2[5] += wb * y[c + 1].y;
+                acc2[6] += wb * y[c + 1].z; acc2[7] += wb * y[c + 1].w;
             }
         }
     }
     Ls_out = Ls + Ls2;
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] += acc2[i];
+}
+
+// Burst plan for the block's range [g0, g1): its pieces (at most four) and
+// the warps dealt to them.  Every piece gets one warp; each further warp goes
+// to the piece whose busiest warp has the most granules, while that is more
+// than one.  A piece's warps take near-equal contiguous shares of it.
+__device__ void make_plan(Plan& pl, const int* sm_pre, const int* sm_len, int rows, int hk, int g0,
+                          int g1, int W, int Geff) {
+    pl.burst = 0;
+    pl.npieces = 0;
+    for (int w = 0; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
+    if (g0 >= g1 || g1 - g0 > kRing) return;
+    int lo = 0, hi = rows - 1;
+    while (lo < hi) {  // largest row with sm_pre[row] <= g0
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
+    }
+    int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+    int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n;
+    int k = 0;
+    for (int g = g0; g < g1;) {
+        if (k == kBurstPieces) return;  // too many pieces: stream mode
+        const int pend = min(g1, us + n);
+        pl.r[k] = r;
+        pl.kvh[k] = kvh;
+        pl.ustart[k] = us;
+        pl.n[k] = n;
+        pl.cstart[k] = owner_of(us, W, Geff);
+        pl.P[k] = owner_of(us + n - 1, W, Geff) - pl.cstart[k] + 1;
+        pl.w0[k] = g;  // piece range [w0, wn) until the warps are dealt below
+        pl.wn[k] = pend;
+        ++k;
+        g = pend;
+        if (g >= g1) break;
+        if (kvh + 1 < hk) {
+            ++kvh;
+            us += n;
+        } else {
+            ++r;
+            while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
+            kvh = 0;
+            n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+            us = sm_pre[r];
+        }
+    }
+    // wc counts the warps of each piece (registers: the loops are unrolled)
+    int wc[kBurstPieces] = {1, 1, 1, 1};
+#pragma unroll
+    for (int e = 1; e < kConsumerWarps; ++e) {
+        if (e < k) continue;
+        int best = -1, bc = 1;
+#pragma unroll
+        for (int i = 0; i < kBurstPieces; ++i) {
+            if (i >= k) break;
+            const int c = (pl.wn[i] - pl.w0[i] + wc[i] - 1) / wc[i];
+            if (c > bc) {
+                bc = c;
+                best = i;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBurstPieces; ++i)
+            if (i == best) ++wc[i];
+    }
+    int w = 0;
+#pragma unroll
+    for (int i = 0; i < kBurstPieces; ++i) {
+        if (i >= k) break;
+        const int a = pl.w0[i], len = pl.wn[i] - a;
+        pl.w0[i] = w;
+        pl.wn[i] = wc[i];
+        for (int j = 0; j < wc[i]; ++j, ++w) {
+            pl.wpiece[w] = i;
+            pl.wa[w] = a + j * len / wc[i];
+            pl.wb[w] = a + (j + 1) * len / wc[i];
+        }
+    }
+    for (; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
+    pl.npieces = k;
+    pl.burst = 1;
+}
+
+// Per-row work of block cta, done by its producer warp after the dependency
+// wait (off the consumers' critical path): rows cta, cta + G, ... with nothing
+// to read get zero outputs, and in the fused form their new token is stored
+// into its slot.  The block that stages the slot's granule takes the token
+// from k_new / v_new directly, so the order of this store and that copy does
+// not matter.
+__device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int lane) {
+    for (int r = cta; r < p.rows; r += G) {
+        if (sm_pre[r + 1] == sm_pre[r])
+            for (int i = lane; i < p.hq * kHeadDim / 8; i += 32)
+                reinterpret_cast<uint4*>(p.out + (int64_t)r * p.hq * kHeadDim)[i] = make_uint4(0, 0, 0, 0);
+        if (!p.positions) continue;
+        const int pos = p.positions[r];
+        if (pos < 0) continue;
+        const int lb = pos / p.bs;
+        if (lb >= p.mbpr) {
+            if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_POSITION);
+            continue;
+        }
+        const int pb = p.tables[(int64_t)r * p.mbpr + lb];
+        if (pb < 0 || pb >= p.nb) {
+            if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+            continue;
+        }
+        const int vecs = p.hk * kHeadDim / 8;
+        const int64_t dst = ((int64_t)pb * p.bs + pos % p.bs) * vecs;
+        for (int i = lane; i < 2 * vecs; i += 32) {
+            if (i < vecs)
+                reinterpret_cast<uint4*>(p.kpool)[dst + i] =
+                    reinterpret_cast<const uint4*>(p.k_new)[(int64_t)r * vecs + i];
+            else
+                reinterpret_cast<uint4*>(p.vpool)[dst + i - vecs] =
+                    reinterpret_cast<const uint4*>(p.v_new)[(int64_t)r * vecs + i - vecs];
+        }
+    }
 }
 
 template <bool kPaged>
@@ -289,9 +579,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* sm_l = sm_m + kConsumerWarps * 8;
     const uint32_t bar_full = sbase + Smem::bars;
     const uint32_t bar_empty = bar_full + kStages * 8;
-    const uint32_t bar_merge = bar_full + 2 * kStages * 8;
+    const uint32_t bar_slot = bar_full + 2 * kStages * 8;
+    const uint32_t bar_merge = bar_slot + kRing * 8;
     int* sm_ppos = reinterpret_cast<int*>(smem + Smem::ppos);
     TileDesc* sm_desc = reinterpret_cast<TileDesc*>(smem + Smem::desc);
+    Plan* sm_plan = reinterpret_cast<Plan*>(smem + Smem::plan);
     volatile int* sm_flags = reinterpret_cast<volatile int*>(smem + Smem::flags);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
     int* sm_pre = reinterpret_cast<int*>(smem + Smem::prefix);
@@ -305,16 +597,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int hk = p.hk;
     const int rows = p.rows;
 
-    // The next kernel in the stream (launched with programmatic serialization)
-    // may start its own prologue now; it waits for this grid before touching
-    // anything this grid writes.
-    if (tid == 0) griddep_launch();
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
+        for (int s = 0; s < kRing; ++s) mbar_init(bar_slot + 8 * s, 1);
         mbar_init(bar_merge, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sm_flags[0] = 0;  // abort
@@ -387,25 +676,85 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int Geff = W < G ? W : G;
     const int g0 = cta < Geff ? (int)((int64_t)W * cta / Geff) : 0;
     const int g1 = cta < Geff ? (int)((int64_t)W * (cta + 1) / Geff) : 0;
+    if (tid == 0) make_plan(*sm_plan, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
+    __syncthreads();
+    const bool burst = sm_plan->burst != 0;
 
     if (warp == kConsumerWarps) {
         // ============================ producer ============================
-        if (g0 >= g1) return;
+        if (g0 >= g1) {
+            griddep_wait();
+            if (kPaged) row_work(p, sm_pre, cta, G, lane);
+            return;
+        }
+        if (burst) {
+            // Every granule of the range goes to its own slot now, before the
+            // dependency wait; lane j handles granule g0 + j.
+            const int ng = g1 - g0;
+            if (lane < ng) {
+                const int gg = g0 + lane;
+                int lo = 0, hi = rows - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
+                }
+                const int r = lo;
+                const int n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+                const int kvh = (gg - sm_pre[r]) / n;
+                const int tok = (gg - sm_pre[r] - kvh * n) * kGranule;
+                int valid = min(kGranule, sm_len[r] - tok);
+                if (valid < 0) valid = 0;
+                bool issue = false;
+                int zrow = 0;
+                if (kPaged) {
+                    const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
+                    if (pb < 0 || pb >= p.nb) {
+                        flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+                        valid = 0;
+                    } else {
+                        zrow = pb * p.bs + tok % p.bs;
+                        issue = true;
+                    }
+                } else {
+                    zrow = r * p.width + tok;
+                    issue = true;
+                }
+                sm_plan->valid[lane] = valid;
+                const uint32_t fb = bar_slot + 8 * lane;
+                mbar_arrive_expect_tx(fb, issue ? kSlotBytes : 0u);
+                if (issue) {
+                    const uint32_t dst = sbase + Smem::ring + lane * kSlotBytes;
+                    tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
+                }
+            }
+            griddep_wait();
+            if (kPaged) row_work(p, sm_pre, cta, G, lane);
+            // Drain: every copy lands before the block exits.
+            for (int j = 0; j < ng; ++j)
+                if (!mbar_wait(bar_slot + 8 * j, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            return;
+        }
         int tile = 0;
         bool waited = false;
         bool aborted = false;
-        // Query copies of tiles armed before the dependency wait (lane 0).
-        uint32_t pq_dst[kStages], pq_bar[kStages];
-        const __half* pq_src[kStages];
-        int npq = 0;
         const uint32_t qbytes = (uint32_t)p.group * 256u;
+        // Stages armed before the dependency wait get their query copies
+        // after it (the query may be written by the preceding kernel).
         auto wait_and_flush = [&]() {
             if (waited) return;
             griddep_wait();
             waited = true;
             if (lane == 0)
-                for (int i = 0; i < npq; ++i) bulk_load(pq_dst[i], pq_src[i], qbytes, pq_bar[i]);
-            npq = 0;
+                for (int t = 0; t < tile && t < kStages; ++t) {
+                    const TileDesc* d = sm_desc + t;
+                    if (d->flags & kFirst)
+                        bulk_load(sbase + Smem::q + t * kQBytes,
+                                  p.q + ((int64_t)d->r * p.hq + d->kvh * p.group) * kHeadDim, qbytes,
+                                  bar_full + 8 * t);
+                }
         };
         for (int bg = g0; bg < g1 && !aborted; bg += 32) {
             const int nbat = min(32, g1 - bg);
@@ -488,29 +837,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, mine && issue));
                 __syncwarp();
                 const uint32_t fb = bar_full + 8 * s;
-                if (lane == 0) mbar_arrive_expect_tx(fb, nissue * 4u * kBoxBytes + (first ? qbytes : 0u));
+                if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kSlotBytes + (first ? qbytes : 0u));
                 __syncwarp();
-                const uint32_t stage = sbase + Smem::stages + s * kStageBytes;
                 if (mine && issue) {
-                    const uint32_t dk = stage + kStageK + (lane - j) * kBoxBytes;
-                    const uint32_t dv = stage + kStageV + (lane - j) * kBoxBytes;
-                    tma_load_3d(dk, &kmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dk + kHalfBytes, &kmap, 64, kvh, zrow, fb);
-                    tma_load_3d(dv, &vmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dv + kHalfBytes, &vmap, 64, kvh, zrow, fb);
+                    const uint32_t dst =
+                        sbase + Smem::ring + (s * kTileGranules + lane - j) * kSlotBytes;
+                    tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
                 }
-                if (first && lane == 0) {
-                    const __half* src = p.q + ((int64_t)r_j * p.hq + kvh_j * p.group) * kHeadDim;
-                    if (waited) {
-                        bulk_load(stage + kStageQ, src, qbytes, fb);
-                    } else {
-                        pq_dst[npq] = stage + kStageQ;
-                        pq_src[npq] = src;
-                        pq_bar[npq] = fb;
-                        ++npq;
-                    }
-                }
-                npq = __shfl_sync(0xffffffffu, npq, 0);
+                if (first && lane == 0 && waited)
+                    bulk_load(sbase + Smem::q + s * kQBytes,
+                              p.q + ((int64_t)r_j * p.hq + kvh_j * p.group) * kHeadDim, qbytes, fb);
                 ++tile;
                 j += ng;
             }
@@ -531,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
             }
         }
+        if (kPaged) row_work(p, sm_pre, cta, G, lane);
         // Drain: the copies of every armed stage land before the block exits.
         for (int t = tile - kStages; t < tile; ++t) {
             if (t < 0) continue;
@@ -541,361 +881,466 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ============================== consumers ==============================
+    if (burst && sm_plan->wpiece[warp] >= 0) {
+        // Warm L2 with this warp's query rows and new token.  A prefetch reads
+        // nothing into the block, so it may precede the dependency wait: the
+        // values used are loaded after it.
+        const int pi = sm_plan->wpiece[warp];
+        const int r = sm_plan->r[pi], kvh = sm_plan->kvh[pi];
+        const char* qrow = reinterpret_cast<const char*>(p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim);
+        if (lane < 2 * p.group)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lane * 128));
+        if (kPaged && p.positions && lane < 8) {
+            const char* nt = reinterpret_cast<const char*>(
+                (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
+        }
+        if (kPaged && p.positions && lane == 8)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.positions + r));
+    }
     // Everything below may read what the preceding kernel wrote (query,
     // positions, new tokens, workspace) or write what it reads.
     griddep_wait();
 
-    if (kPaged) {
-        for (int r = cta; r < rows; r += G) {
-            // Rows with nothing to read get zeros.
-            if (sm_pre[r + 1] == sm_pre[r])
-                for (int i = tid; i < p.hq * kHeadDim / 8; i += kConsumers)
-                    reinterpret_cast<uint4*>(p.out + (int64_t)r * p.hq * kHeadDim)[i] =
-                        make_uint4(0, 0, 0, 0);
-            // Fused append: this block stores row r's new token into its slot.
-            if (p.positions) {
-                const int pos = p.positions[r];
-                if (pos >= 0) {
-                    const int lb = pos / p.bs;
-                    int pb = -1;
-                    if (lb >= p.mbpr) {
-                        if (tid == 0) flag_error(p.dev_err, PKV_DEV_ERR_POSITION);
-                    } else {
-                        pb = p.tables[(int64_t)r * p.mbpr + lb];
-                        if ((pb < 0 || pb >= p.nb) && tid == 0) flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-                    }
-                    if (pb >= 0 && pb < p.nb) {
-                        const int vecs = hk * kHeadDim / 8;
-                        const int64_t dst = ((int64_t)pb * p.bs + pos % p.bs) * vecs;
-                        for (int i = tid; i < 2 * vecs; i += kConsumers) {
-                            if (i < vecs)
-                                reinterpret_cast<uint4*>(p.kpool)[dst + i] =
-                                    reinterpret_cast<const uint4*>(p.k_new)[(int64_t)r * vecs + i];
-                            else
-                                reinterpret_cast<uint4*>(p.vpool)[dst + i - vecs] =
-                                    reinterpret_cast<const uint4*>(p.v_new)[(int64_t)r * vecs + i - vecs];
-                        }
-                    }
-                }
-            }
-        }
-    }
     if (g0 >= g1) return;
 
-    // Append positions of this block's first pieces, read once right after
-    // the wait, so a piece never starts with a dependent global load.
     const bool fused = kPaged && p.positions != nullptr;
-    if (fused) {
-        if (tid == 0) {
-            int lo = 0, hi = rows - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
-            }
-            int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-            int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n, k = 0;
-            for (int g = g0; g < g1 && k < kMaxPieces;) {
-                sm_ppos[k++] = r;  // row of piece k (replaced by its position below)
-                g = min(g1, us + n);
-                if (g >= g1) break;
-                if (kvh + 1 < hk) {
-                    ++kvh;
-                    us += n;
-                } else {
-                    ++r;
-                    while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
-                    kvh = 0;
-                    n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                    us = sm_pre[r];
-                }
-            }
-            sm_flags[2] = k;
-        }
-        consumer_sync();
-    }
-    // Each thread's position load stays in flight while the first tile lands;
-    // it is published to shared memory after the first full barrier.
-    const int npp = fused ? sm_flags[2] : 0;
-    const int my_pos = tid < npp ? p.positions[sm_ppos[tid]] : 0;
-    bool pos_published = !fused;
-    int piece = 0;
-
     const int gq = lane >> 2;  // MMA group id: token row (QK) / dim row (PV) / head (B frag)
     const int tq = lane & 3;   // thread in group
-    uint32_t qb[16];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[8][4];
-    int patch_tok = -1;        // unit-local token this piece must take from k_new / v_new
-    uint4 patch_val = make_uint4(0, 0, 0, 0);
-    int tile = 0;
-    while (true) {
-        const int s = tile % kStages;
-        const uint32_t round = (uint32_t)tile / kStages;
-        if (!mbar_wait(bar_full + 8 * s, round & 1)) {
-            if (lane == 0) {
-                sm_flags[0] = 1;
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            }
-            break;
-        }
-        if (!pos_published) {
-            if (tid < npp) sm_ppos[tid] = my_pos;
-            consumer_sync();
-            pos_published = true;
-        }
-        const TileDesc* d = sm_desc + s;
-        const int flags = d->flags;
-        if (flags & kEnd) break;
-        const int r = d->r, kvh = d->kvh, ng = d->ng, tok0 = d->tok0;
-        const int ustart = d->ustart, n = d->n, pend = d->pend;
-        const int valid = warp < ng ? d->valid[warp] : 0;
-        const uint32_t stage = sbase + Smem::stages + s * kStageBytes;
-        unsigned char* stage_ptr = smem + Smem::stages + s * kStageBytes;
-        if (flags & kFirst) {
-            // B fragments of Q^T: b0 = Q[head gq][16ks + 2tq..], b1 = Q[head gq][16ks + 8 + 2tq..]
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(stage_ptr + kStageQ + gq * 256);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qb[2 * ks] = gq < p.group ? qrow[ks * 8 + tq] : 0u;
-                qb[2 * ks + 1] = gq < p.group ? qrow[ks * 8 + 4 + tq] : 0u;
-            }
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-            patch_tok = -1;
-            const int this_piece = piece++;
-            if (fused) {
-                // The appended token, if it falls inside this piece, is taken from
-                // k_new / v_new (its slot may be written concurrently).
-                const int pos = this_piece < kMaxPieces ? sm_ppos[this_piece] : p.positions[r];
-                const int pg = pos >= 0 ? ustart + pos / kGranule : -1;
-                if (pos >= 0 && pg >= ustart + tok0 / kGranule && pg < pend) {
-                    patch_tok = pos;
-                    const int chunk = lane & 15;
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
-                    patch_val = src[chunk];
-                }
-            }
-        }
-        if (warp < ng) {
-            const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
-            const uint32_t kb = stage + kStageK + warp * kBoxBytes;
-            const uint32_t vb = stage + kStageV + warp * kBoxBytes;
-            bool wrote = false;
-            if (valid < kGranule) {
-                // Rows past the row's length (or of a skipped block) may hold
-                // anything, NaN included: zero them so 0 * V stays 0.
-                uint4* v0 = reinterpret_cast<uint4*>(stage_ptr + kStageV + warp * kBoxBytes);
-                for (int i = lane; i < (kGranule - valid) * 8; i += 32) {
-                    const int row = valid + (i >> 3);
-                    v0[row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
-                    v0[kHalfBytes / 16 + row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
-                }
-                wrote = true;
-            }
-            if (patch_tok >= gtok && patch_tok < gtok + valid) {
-                // Overwrite the staged row with the new token (swizzled layout).
-                const int row = patch_tok - gtok;
-                const int c16 = lane & 15;  // 16-byte chunk of the 128 dims
-                unsigned char* box = stage_ptr + (lane < 16 ? kStageK : kStageV) + warp * kBoxBytes +
-                                     (c16 >> 3) * kHalfBytes;
-                *reinterpret_cast<uint4*>(box + row * 128 + (((c16 & 7) ^ (row & 7)) << 4)) = patch_val;
-                wrote = true;
-            }
-            if (wrote) __syncwarp();
-            // ---- S^T = K . Q^T ----
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+
+    if (burst) {
+        // ============================ burst mode ============================
+        const Plan& pl = *sm_plan;
+        const int pi = pl.wpiece[warp];
+        if (pi >= 0) {
+            const int r = pl.r[pi], kvh = pl.kvh[pi], us = pl.ustart[pi];
+            const int a = pl.wa[warp], b = pl.wb[warp];
+            // Query fragments straight from global memory: b0 = Q[head gq][16ks + 2tq..],
+            // b1 = Q[head gq][16ks + 8 + 2tq..].
+            uint32_t qb[16];
             {
-                // two independent accumulation chains (even / odd k-steps)
-                float sd[4] = {0.f, 0.f, 0.f, 0.f};
-                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                    p.q + ((int64_t)r * p.hq + kvh * p.group + gq) * kHeadDim);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const int chunk = (ks & 3) * 2 + (lane >> 4);
-                    const uint32_t addr =
-                        kb + (ks >> 2) * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(addr, a0, a1, a2, a3);
-                    mma16816((ks & 1) ? sd : sc, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
+                    qb[2 * ks] = gq < p.group ? qrow[ks * 8 + tq] : 0u;
+                    qb[2 * ks + 1] = gq < p.group ? qrow[ks * 8 + 4 + tq] : 0u;
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sc[i] += sd[i];
             }
-            // scores: sc0 = (tok gq, head 2tq), sc1 = (gq, 2tq+1), sc2/3 = tok gq+8
-            const float s0 = gq < valid ? sc[0] * p.scale_log2 : -INFINITY;
-            const float s1 = gq < valid ? sc[1] * p.scale_log2 : -INFINITY;
-            const float s2 = gq + 8 < valid ? sc[2] * p.scale_log2 : -INFINITY;
-            const float s3 = gq + 8 < valid ? sc[3] * p.scale_log2 : -INFINITY;
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+            // The appended token, if it falls inside this warp's granules, is
+            // taken from k_new / v_new (its slot may be written concurrently).
+            int patch_tok = -1;
+            uint4 patch_val = make_uint4(0, 0, 0, 0);
+            if (fused) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
+                patch_val = src[lane & 15];
+                const int pos = p.positions[r];
+                if (pos >= 0 && us + pos / kGranule >= a && us + pos / kGranule < b) patch_tok = pos;
+            }
+            Soft st;
+            st.reset();
+            bool ok = true;
+            for (int bs = a; bs < b && ok; bs += kBatch) {
+                const int nb = min(kBatch, b - bs);
+                uint32_t slot[kBatch];
+                int valid[kBatch];
+                bool wrote = false;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    slot[j] = sbase;
+                    valid[j] = 0;
+                    if (j >= nb || !ok) continue;
+                    const int si = bs + j - g0;
+                    if (!mbar_wait(bar_slot + 8 * si, 0)) {
+                        if (lane == 0) {
+                            sm_flags[0] = 1;
+                            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+                        }
+                        ok = false;
+                        continue;
+                    }
+                    slot[j] = sbase + Smem::ring + si * kSlotBytes;
+                    valid[j] = pl.valid[si];
+                    const int gtok = (bs + j - us) * kGranule;
+                    wrote |= prepare_granule(smem + Smem::ring + si * kSlotBytes, valid[j],
+                                             patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
+                }
+                if (!ok) break;
+                if (wrote) __syncwarp();
+                if (nb == 3)
+                    attend<3>(st, qb, slot, valid, p.scale_log2, lane);
+                else if (nb == 2)
+                    attend<2>(st, qb, slot, valid, p.scale_log2, lane);
+                else
+                    attend<1>(st, qb, slot, valid, p.scale_log2, lane);
+            }
+            // Dump the warp's state into its first slot: m[8], l[8], o[8][132].
+            __syncwarp();
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+                st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
-            const uint32_t px = pack_half2(fast_exp2(s0 - mu0), fast_exp2(s1 - mu1));
-            const uint32_t py = pack_half2(fast_exp2(s2 - mu0), fast_exp2(s3 - mu1));
-            {
-                const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&px));
-                const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&py));
-                l0 = l0 * al0 + fx.x + fy.x;
-                l1 = l1 * al1 + fx.y + fy.y;
+            float* dump = reinterpret_cast<float*>(smem + Smem::ring + (a - g0) * kSlotBytes);
+            if (gq == 0) {
+                dump[2 * tq] = st.m0;
+                dump[2 * tq + 1] = st.m1;
+                dump[8 + 2 * tq] = st.l0;
+                dump[8 + 2 * tq + 1] = st.l1;
             }
+            float* o0 = dump + kRecHead;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o[i][0] *= al0;
-                o[i][1] *= al1;
-                o[i][2] *= al0;
-                o[i][3] *= al1;
+            for (int mt = 0; mt < 8; ++mt) {
+                const int dim = mt * 16 + gq;
+                o0[(2 * tq) * kDumpStride + dim] = st.o[mt][0];
+                o0[(2 * tq + 1) * kDumpStride + dim] = st.o[mt][1];
+                o0[(2 * tq) * kDumpStride + dim + 8] = st.o[mt][2];
+                o0[(2 * tq + 1) * kDumpStride + dim + 8] = st.o[mt][3];
             }
-            // B fragments of P^T (token x head) by transposing in registers.
-            const uint32_t pb0 = movmatrix_t(px);
-            const uint32_t pb1 = movmatrix_t(py);
-            // ---- O^T += V^T . P^T ----
-            {
-                const int row = (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
-                    const uint32_t addr =
-                        vb + (mt >> 2) * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(addr, a0, a1, a2, a3);
-                    mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-                }
-            }
-            // Generic-proxy writes must be ordered before TMA reuses the stage.
-            if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        ++tile;
-        if (!(flags & kLast)) continue;
-
-        // ---- end of a piece: combine the four warps' partial softmax states ----
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
-        if (gq == 0) {
-            sm_m[warp * 8 + 2 * tq] = m0;
-            sm_m[warp * 8 + 2 * tq + 1] = m1;
-            sm_l[warp * 8 + 2 * tq] = l0;
-            sm_l[warp * 8 + 2 * tq + 1] = l1;
-        }
-        const int uend = ustart + n;
-        const int cstart = owner_of(ustart, W, Geff);
-        const int P = owner_of(uend - 1, W, Geff) - cstart + 1;
-        const int u = r * hk + kvh;
-        const int my_slot = cta + u;  // piece slot: block + unit is unique
         consumer_sync();
-        const int ch = tid >> 4;        // head this thread combines
-        float Mh = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, sm_m[w * 8 + ch]);
-        float wsc[kConsumerWarps];
-        float Lh = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            wsc[w] = Mh == -INFINITY ? 0.f : fast_exp2(sm_m[w * 8 + ch] - Mh);
-            Lh += wsc[w] * sm_l[w * 8 + ch];
-        }
-        float* rec = p.records + (int64_t)my_slot * p.rec_floats;
-        if (P > 1 && (tid & 15) == 0 && ch < p.group) {
-            rec[ch] = Mh;
-            rec[8 + ch] = Lh;
-        }
-        const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
-        const int cq = (tid & 15) * 4;  // four dims within a 64-dim pass
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            // warp writes its O^T fragments for dims [64 pass, 64 pass + 64)
-            float* base = sm_comb + warp * 8 * kCombStride;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int mt = 4 * pass + k;
-                base[(2 * tq) * kCombStride + 16 * k + gq] = o[mt][0];
-                base[(2 * tq + 1) * kCombStride + 16 * k + gq] = o[mt][1];
-                base[(2 * tq) * kCombStride + 16 * k + gq + 8] = o[mt][2];
-                base[(2 * tq + 1) * kCombStride + 16 * k + gq + 8] = o[mt][3];
-            }
-            consumer_sync();
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        // The next kernel in the stream (launched with programmatic
+        // serialization) may start now that this block's queries have
+        // arrived: its prefetch then no longer competes with them.  It waits
+        // for this grid before touching anything this grid writes.
+        if (tid == 0) griddep_launch();
+        if (sm_flags[0]) return;
+        // Combine every piece's warp states.  Thread (head h, dims 8c..8c+7)
+        // reads all four warps' states at once, then finishes each piece.
+        {
+            const int gsz = p.group;
+            const int h = tid >> 4, c = tid & 15;
+            float mw[kConsumerWarps], lw[kConsumerWarps];
+            float4 xw[kConsumerWarps], yw[kConsumerWarps];
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float4 x =
-                    *reinterpret_cast<const float4*>(sm_comb + (w * 8 + ch) * kCombStride + cq);
-                v.x += wsc[w] * x.x;
-                v.y += wsc[w] * x.y;
-                v.z += wsc[w] * x.z;
-                v.w += wsc[w] * x.w;
-            }
-            const int dd = 64 * pass + cq;
-            if (ch < p.group) {
-                if (P == 1) {
-                    uint2 pk;
-                    pk.x = pack_half2(v.x * inv, v.y * inv);
-                    pk.y = pack_half2(v.z * inv, v.w * inv);
-                    *reinterpret_cast<uint2*>(
-                        p.out + ((int64_t)r * p.hq + kvh * p.group + ch) * kHeadDim + dd) = pk;
-                } else {
-                    *reinterpret_cast<float4*>(rec + kRecHead + ch * kHeadDim + dd) = v;
+                mw[w] = -INFINITY;
+                lw[w] = 0.f;
+                xw[w] = yw[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (pl.wpiece[w] >= 0 && h < gsz) {
+                    const float* dw = reinterpret_cast<const float*>(smem + Smem::ring +
+                                                                     (pl.wa[w] - g0) * kSlotBytes);
+                    mw[w] = dw[h];
+                    lw[w] = dw[8 + h];
+                    xw[w] = *reinterpret_cast<const float4*>(dw + kRecHead + h * kDumpStride + 8 * c);
+                    yw[w] = *reinterpret_cast<const float4*>(dw + kRecHead + h * kDumpStride + 8 * c + 4);
                 }
+            }
+#pragma unroll
+            for (int pc = 0; pc < kBurstPieces; ++pc) {
+                if (pc >= pl.npieces || h >= gsz) break;
+                const int w0 = pl.w0[pc], w1 = w0 + pl.wn[pc];
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    if (w >= w0 && w < w1) M = fmaxf(M, mw[w]);
+                float L = 0.f, acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    if (w < w0 || w >= w1) continue;
+                    const float wt = M == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
+                    L += wt * lw[w];
+                    acc[0] += wt * xw[w].x; acc[1] += wt * xw[w].y; acc[2] += wt * xw[w].z; acc[3] += wt * xw[w].w;
+                    acc[4] += wt * yw[w].x; acc[5] += wt * yw[w].y; acc[6] += wt * yw[w].z; acc[7] += wt * yw[w].w;
+                }
+                const int r = pl.r[pc], kvh = pl.kvh[pc];
+                if (pl.P[pc] == 1) {
+                    const float inv = L > 0.f ? __fdividef(1.f, L) : 0.f;
+                    uint4 pk;
+                    pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
+                    pk.y = pack_half2(acc[2] * inv, acc[3] * inv);
+                    pk.z = pack_half2(acc[4] * inv, acc[5] * inv);
+                    pk.w = pack_half2(acc[6] * inv, acc[7] * inv);
+                    *reinterpret_cast<uint4*>(p.out + ((int64_t)r * p.hq + kvh * gsz + h) * kHeadDim + 8 * c) = pk;
+                } else {
+                    float* rec = p.records + (int64_t)(cta + r * hk + kvh) * p.rec_floats;
+                    if (c == 0) {
+                        rec[h] = M;
+                        rec[8 + h] = L;
+                    }
+                    *reinterpret_cast<float4*>(rec + kRecHead + h * kHeadDim + 8 * c) =
+                        make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    *reinterpret_cast<float4*>(rec + kRecHead + h * kHeadDim + 8 * c + 4) =
+                        make_float4(acc[4], acc[5], acc[6], acc[7]);
+                }
+            }
+        }
+        if (tid == 0) {
+            int k = 0;
+            for (int pc = 0; pc < pl.npieces; ++pc) {
+                if (pl.P[pc] == 1) continue;
+                sm_flags[4 + 5 * k] = pl.r[pc] * hk + pl.kvh[pc];
+                sm_flags[5 + 5 * k] = pl.cstart[pc];
+                sm_flags[6 + 5 * k] = pl.P[pc];
+                sm_flags[7 + 5 * k] = pl.r[pc];
+                sm_flags[8 + 5 * k] = pl.kvh[pc];
+                ++k;
+            }
+            sm_flags[3] = k;
+        }
+    } else {
+        // ============================ stream mode ============================
+        // Append positions of this block's first pieces, read once right after
+        // the wait, so a piece never starts with a dependent global load.
+        if (fused) {
+            if (tid == 0) {
+                int lo = 0, hi = rows - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
+                }
+                int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+                int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n, k = 0;
+                for (int g = g0; g < g1 && k < kMaxPieces;) {
+                    sm_ppos[k++] = r;  // row of piece k (replaced by its position below)
+                    g = min(g1, us + n);
+                    if (g >= g1) break;
+                    if (kvh + 1 < hk) {
+                        ++kvh;
+                        us += n;
+                    } else {
+                        ++r;
+                        while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
+                        kvh = 0;
+                        n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+                        us = sm_pre[r];
+                    }
+                }
+                sm_flags[2] = k;
             }
             consumer_sync();
         }
-        if (P == 1) continue;
-        // A split piece: its record is published; its arrival is counted once
-        // per block, after the block's last piece (a contiguous range has at
-        // most two split pieces: its first and its last).
-        if (tid == 0) {
-            const int k = sm_flags[3];
-            sm_flags[4 + 5 * k] = u;
-            sm_flags[5 + 5 * k] = cstart;
-            sm_flags[6 + 5 * k] = P;
-            sm_flags[7 + 5 * k] = r;
-            sm_flags[8 + 5 * k] = kvh;
-            sm_flags[3] = k + 1;
+        // Each thread's position load stays in flight while the first tile lands;
+        // it is published to shared memory after the first full barrier.
+        const int npp = fused ? sm_flags[2] : 0;
+        const int my_pos = tid < npp ? p.positions[sm_ppos[tid]] : 0;
+        bool pos_published = !fused;
+        int piece = 0;
+
+        uint32_t qb[16];
+        Soft st;
+        st.reset();
+        int patch_tok = -1;        // unit-local token this piece must take from k_new / v_new
+        uint4 patch_val = make_uint4(0, 0, 0, 0);
+        int tile = 0;
+        while (true) {
+            const int s = tile % kStages;
+            const uint32_t round = (uint32_t)tile / kStages;
+            if (!mbar_wait(bar_full + 8 * s, round & 1)) {
+                if (lane == 0) {
+                    sm_flags[0] = 1;
+                    flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+                }
+                break;
+            }
+            if (!pos_published) {
+                if (tid < npp) sm_ppos[tid] = my_pos;
+                consumer_sync();
+                pos_published = true;
+            }
+            const TileDesc* d = sm_desc + s;
+            const int flags = d->flags;
+            if (flags & kEnd) break;
+            const int r = d->r, kvh = d->kvh, ng = d->ng, tok0 = d->tok0;
+            const int ustart = d->ustart, n = d->n, pend = d->pend;
+            const int valid = warp < ng ? d->valid[warp] : 0;
+            if (flags & kFirst) {
+                // B fragments of Q^T: b0 = Q[head gq][16ks + 2tq..], b1 = Q[head gq][16ks + 8 + 2tq..]
+                const uint32_t* qrow =
+                    reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qb[2 * ks] = gq < p.group ? qrow[ks * 8 + tq] : 0u;
+                    qb[2 * ks + 1] = gq < p.group ? qrow[ks * 8 + 4 + tq] : 0u;
+                }
+                st.reset();
+                patch_tok = -1;
+                const int this_piece = piece++;
+                if (fused) {
+                    // The appended token, if it falls inside this piece, is taken from
+                    // k_new / v_new (its slot may be written concurrently).
+                    const int pos = this_piece < kMaxPieces ? sm_ppos[this_piece] : p.positions[r];
+                    const int pg = pos >= 0 ? ustart + pos / kGranule : -1;
+                    if (pos >= 0 && pg >= ustart + tok0 / kGranule && pg < pend) {
+                        patch_tok = pos;
+                        const int chunk = lane & 15;
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
+                        patch_val = src[chunk];
+                    }
+                }
+            }
+            if (warp < ng) {
+                const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
+                const int si = s * kTileGranules + warp;
+                const bool wrote = prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
+                                                   patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
+                if (wrote) __syncwarp();
+                const uint32_t slot[1] = {sbase + Smem::ring + si * kSlotBytes};
+                const int vv[1] = {valid};
+                attend<1>(st, qb, slot, vv, p.scale_log2, lane);
+                // Generic-proxy writes must be ordered before TMA reuses the slot.
+                if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            if (tile == 0 && tid == 0) griddep_launch();  // as in burst mode
+            ++tile;
+            if (!(flags & kLast)) continue;
+
+            // ---- end of a piece: combine the four warps' partial softmax states ----
+            float l0 = st.l0, l1 = st.l1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            if (gq == 0) {
+                sm_m[warp * 8 + 2 * tq] = st.m0;
+                sm_m[warp * 8 + 2 * tq + 1] = st.m1;
+                sm_l[warp * 8 + 2 * tq] = l0;
+                sm_l[warp * 8 + 2 * tq + 1] = l1;
+            }
+            const int uend = ustart + n;
+            const int cstart = owner_of(ustart, W, Geff);
+            const int P = owner_of(uend - 1, W, Geff) - cstart + 1;
+            const int u = r * hk + kvh;
+            const int my_slot = cta + u;  // piece slot: block + unit is unique
+            consumer_sync();
+            const int ch = tid >> 4;        // head this thread combines
+            float Mh = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, sm_m[w * 8 + ch]);
+            float wsc[kConsumerWarps];
+            float Lh = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                wsc[w] = Mh == -INFINITY ? 0.f : fast_exp2(sm_m[w * 8 + ch] - Mh);
+                Lh += wsc[w] * sm_l[w * 8 + ch];
+            }
+            float* rec = p.records + (int64_t)my_slot * p.rec_floats;
+            if (P > 1 && (tid & 15) == 0 && ch < p.group) {
+                rec[ch] = Mh;
+                rec[8 + ch] = Lh;
+            }
+            const float inv = Lh > 0.f ? __fdividef(1.f, Lh) : 0.f;
+            const int cq = (tid & 15) * 4;  // four dims within a 64-dim pass
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                // warp writes its O^T fragments for dims [64 pass, 64 pass + 64)
+                float* base = sm_comb + warp * 8 * kCombStride;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int mt = 4 * pass + k;
+                    base[(2 * tq) * kCombStride + 16 * k + gq] = st.o[mt][0];
+                    base[(2 * tq + 1) * kCombStride + 16 * k + gq] = st.o[mt][1];
+                    base[(2 * tq) * kCombStride + 16 * k + gq + 8] = st.o[mt][2];
+                    base[(2 * tq + 1) * kCombStride + 16 * k + gq + 8] = st.o[mt][3];
+                }
+                consumer_sync();
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float4 x =
+                        *reinterpret_cast<const float4*>(sm_comb + (w * 8 + ch) * kCombStride + cq);
+                    v.x += wsc[w] * x.x;
+                    v.y += wsc[w] * x.y;
+                    v.z += wsc[w] * x.z;
+                    v.w += wsc[w] * x.w;
+                }
+                const int dd = 64 * pass + cq;
+                if (ch < p.group) {
+                    if (P == 1) {
+                        uint2 pk;
+                        pk.x = pack_half2(v.x * inv, v.y * inv);
+                        pk.y = pack_half2(v.z * inv, v.w * inv);
+                        *reinterpret_cast<uint2*>(
+                            p.out + ((int64_t)r * p.hq + kvh * p.group + ch) * kHeadDim + dd) = pk;
+                    } else {
+                        *reinterpret_cast<float4*>(rec + kRecHead + ch * kHeadDim + dd) = v;
+                    }
+                }
+                consumer_sync();
+            }
+            if (P == 1) continue;
+            // A split piece: its record is published; its arrival is counted once
+            // per block, after the block's last piece (a contiguous range has at
+            // most two split pieces: its first and its last).
+            if (tid == 0) {
+                const int k = sm_flags[3];
+                sm_flags[4 + 5 * k] = u;
+                sm_flags[5 + 5 * k] = cstart;
+                sm_flags[6 + 5 * k] = P;
+                sm_flags[7 + 5 * k] = r;
+                sm_flags[8 + 5 * k] = kvh;
+                sm_flags[3] = k + 1;
+            }
         }
     }
 
-    // ---- arrivals of this block's split pieces; the last arriver of a unit
-    // merges its pieces through their log-sum-exp and writes the output ----
+    // ---- split pieces: every piece's record is published; the block that
+    // holds a unit's last piece waits for the others and merges the unit
+    // through the log-sum-exp of all its records (a block holds the last
+    // piece of at most one split unit: its first piece) ----
+    // Shared memory written through the generic proxy (partials, patches) is
+    // ordered before the bulk copies that may land records over it.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     consumer_sync();
     const int nsplit = sm_flags[3];
     if (nsplit == 0 || sm_flags[0]) return;
-    __threadfence();  // the records are visible before the arrivals count
+    // Records written here through the generic proxy may be read back by the
+    // bulk copies of the landing below.
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     consumer_sync();
     if (tid < nsplit) {
+        // The barrier above orders every thread's record stores before this
+        // thread's release.
         const int u = sm_flags[4 + 5 * tid];
+        const int cs = sm_flags[5 + 5 * tid];
         const int P = sm_flags[6 + 5 * tid];
-        const int prev = atomicAdd(p.counters + u, 1);
-        const int last = prev == P - 1;
-        if (last) p.counters[u] = 0;  // every piece has arrived: re-arm for the next call
-        sm_flags[14 + tid] = last;
+        int* ctr = p.counters + (int64_t)u * kCounterStride;
+        int merge = 0;
+        if (cta != cs + P - 1) {
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
+        } else {
+            // Bounded wait for the other P - 1 pieces; the acquire makes their
+            // records visible to this block after the next barrier.
+            int seen = 0;
+            for (uint32_t i = 0; i < kPollLimit; ++i) {
+                asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+                if (seen >= P - 1) break;
+                __nanosleep(32);
+            }
+            if (seen >= P - 1) {
+                // with the relaxed read that saw every release, this fence
+                // makes the pieces' records visible
+                *ctr = 0;  // every piece has arrived: re-arm for the next call
+                merge = 1;
+            } else {
+                sm_flags[0] = 1;
+                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            }
+        }
+        sm_flags[14 + tid] = merge;
     }
     consumer_sync();
-    __threadfence();
+    if (sm_flags[0]) return;
     const uint32_t rec_bytes = (uint32_t)p.rec_floats * 4u;
     uint32_t land_total = 0;
     for (int k = 0; k < nsplit; ++k)
         if (sm_flags[14 + k]) land_total += (uint32_t)sm_flags[6 + 5 * k] * rec_bytes;
     if (land_total == 0) return;
-    // The stages are idle once the block's tiles are consumed: every child
+    // The ring is idle once the block's granules are consumed: every child
     // record of the units merged here comes in by bulk copies at once.
-    const bool landing = land_total <= (uint32_t)(kStages * kStageBytes);
+    // The ring is idle once the block's granules are consumed: the records
+    // of the merged unit land there by bulk copies issued at once.
+    const bool landing = land_total <= (uint32_t)(kRing * kSlotBytes);
     if (landing) {
         if (warp == 0) {
             asm volatile("fence.proxy.async.global;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (lane == 0) mbar_arrive_expect_tx(bar_merge, land_total);
             __syncwarp();
             uint32_t off = 0;
@@ -903,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!sm_flags[14 + k]) continue;
                 const int u = sm_flags[4 + 5 * k], cs = sm_flags[5 + 5 * k], P = sm_flags[6 + 5 * k];
                 for (int j = lane; j < P; j += 32)
-                    bulk_load(sbase + Smem::stages + off + j * rec_bytes,
+                    bulk_load(sbase + Smem::ring + off + j * rec_bytes,
                               p.records + (int64_t)(cs + j + u) * p.rec_floats, rec_bytes, bar_merge);
                 off += (uint32_t)P * rec_bytes;
             }
@@ -922,13 +1367,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r = sm_flags[7 + 5 * k], kvh = sm_flags[8 + 5 * k];
         if (mh < p.group) {
             float Ls = 0.f, acc[8];
-            const float* land = reinterpret_cast<const float*>(smem + Smem::stages + off);
+            const float* land = reinterpret_cast<const float*>(smem + Smem::ring + off);
             const float* glob = p.records + (int64_t)(cs + u) * p.rec_floats;
             if (landing)
-                merge_children(land, P, p.rec_floats, mh, md, false, Ls, acc);
+                merge_children<false>(land, P, p.rec_floats, mh, md, Ls, acc);
             else
-                merge_children(glob, P, p.rec_floats, mh, md, true, Ls, acc);
-            const float iv = Ls > 0.f ? 1.f / Ls : 0.f;
+                merge_children<true>(glob, P, p.rec_floats, mh, md, Ls, acc);
+            const float iv = Ls > 0.f ? __fdividef(1.f, Ls) : 0.f;
             uint4 pk;
             pk.x = pack_half2(acc[0] * iv, acc[1] * iv);
             pk.y = pack_half2(acc[2] * iv, acc[3] * iv);
@@ -1039,7 +1484,9 @@ static int64_t tma_slots(int rows, int kv_heads, int max_seq_len) {
 }
 
 static size_t tma_counter_bytes(int rows, int kv_heads) {
-    return align_up(sizeof(int) * (size_t)rows * (size_t)kv_heads, 256);
+    // one counter per 128-byte line: arrivals on different units never
+    // queue on the same L2 line
+    return align_up((size_t)tma::kCounterStride * sizeof(int) * (size_t)rows * (size_t)kv_heads, 256);
 }
 
 size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len) {
