@@ -85,6 +85,16 @@ def _load():
             lib.oracle_copy_blocks.restype = I
             lib.oracle_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I]
             lib.oracle_prefill_scatter.restype = I
+            lib.oracle_fp8_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_fp8_e4m3_to_double.restype = D
+            lib.oracle_fp8_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_fp8_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_fp8_quantize_array.argtypes = [P, P, ctypes.c_int64, ctypes.c_float]
+            lib.oracle_fp8_quantize_array.restype = None
+            lib.oracle_paged_append_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I]
+            lib.oracle_paged_append_fp8.restype = I
+            lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, I, I]
+            lib.oracle_paged_decode_fp8.restype = I
             _lib = lib
     return _lib
 
@@ -213,3 +223,73 @@ def prefill_scatter(k_pool, v_pool, block_tables, src_start, dst_start, lengths,
                                         _ptr(ks), _ptr(vs), rows, width, hk, d, bs, bt.shape[1], nb)
     _check(rc, "prefill_scatter")
     return kp, vp
+
+
+# --- FP8 (E4M3) pools, one scale per KV head ------------------------------------
+
+def fp8_e4m3_to_double(codes) -> np.ndarray:
+    """Exact E4M3 decode of uint8 codes (written from the format definition)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    L = _load()
+    return np.vectorize(lambda v: L.oracle_fp8_e4m3_to_double(int(v)), otypes=[np.float64])(c) \
+        if c.size else np.zeros(c.shape)
+
+
+def fp8_e4m3_from_float(values) -> np.ndarray:
+    """Nearest E4M3 codes of float32 values (ties to even, saturating at 448)."""
+    v = np.asarray(values, dtype=np.float32)
+    L = _load()
+    return np.vectorize(lambda x: L.oracle_fp8_e4m3_from_float(float(x)), otypes=[np.uint8])(v) \
+        if v.size else np.zeros(v.shape, dtype=np.uint8)
+
+
+def fp8_quantize(x_fp16, scale: float) -> np.ndarray:
+    """Codes of fp16 values quantised with one scale (binary32 x / scale, then encode)."""
+    b = _bits(x_fp16)
+    out = np.empty(b.shape, dtype=np.uint8)
+    _load().oracle_fp8_quantize_array(_ptr(out), _ptr(b), b.size, float(np.float32(scale)))
+    return out
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _u8(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected uint8 fp8 codes, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def paged_append_fp8(k_pool8, v_pool8, k_scale, v_scale, block_tables, positions, k_new, v_new):
+    """Copies of the FP8 pools with each row's new token quantised into its slot."""
+    kp = _u8(k_pool8).copy(); vp = _u8(v_pool8).copy()
+    ks = _f32(k_scale); vs = _f32(v_scale)
+    bt = _i32(block_tables); pos = _i32(positions)
+    kn = _bits(k_new); vn = _bits(v_new)
+    nb, bs, hk, d = kp.shape
+    rows = pos.shape[0]
+    assert kn.shape == (rows, hk, d) and vn.shape == kn.shape and ks.shape == (hk,)
+    rc = _load().oracle_paged_append_fp8(_ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(pos),
+                                         _ptr(kn), _ptr(vn), rows, hk, d, bs,
+                                         bt.shape[1] if bt.ndim == 2 else 0, nb)
+    _check(rc, "paged_append_fp8")
+    return kp, vp
+
+
+def paged_decode_fp8(q, k_pool8, v_pool8, k_scale, v_scale, block_tables, seq_lens, scale: float,
+                     num_threads: int = 1) -> np.ndarray:
+    """fp64 attention over FP8 pools dequantised with one scale per KV head."""
+    q = _bits(q); kp = _u8(k_pool8); vp = _u8(v_pool8)
+    ks = _f32(k_scale); vs = _f32(v_scale)
+    bt = _i32(block_tables); sl = _i32(seq_lens)
+    rows, hq, d = q.shape
+    nb, bs, hk, d2 = kp.shape
+    assert d2 == d and vp.shape == kp.shape and ks.shape == (hk,) and vs.shape == (hk,)
+    out = np.zeros((rows, hq, d), dtype=np.float64)
+    rc = _load().oracle_paged_decode_fp8(_ptr(out), _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs),
+                                         _ptr(bt), _ptr(sl), rows, hq, hk, d, bs, float(scale),
+                                         bt.shape[1], nb, int(num_threads))
+    _check(rc, "paged_decode_fp8")
+    return out

@@ -411,3 +411,168 @@ int oracle_prefill_scatter(uint16_t* k_pool, uint16_t* v_pool, const int32_t* bl
     }
     return ORACLE_OK;
 }
+
+/*
+ * FP8 KV pools.  "PagedAttention" (deepconcepts.dev), section "Checking it
+ * on a real system", names FP8 KV as a way to change the bytes per token;
+ * the pages fix no format.  The reading taken here: the OCP 8-bit floating
+ * point E4M3 format, one float scale per KV head (given by the caller); a
+ * stored code c stands for e4m3(c) * scale[head].
+ *
+ * E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent 0
+ * is subnormal: mantissa * 2^-9.  Otherwise (8 + mantissa) * 2^(exponent-10).
+ * The codes with all exponent and mantissa bits set (0x7F, 0xFF) are NaN;
+ * there is no infinity, so the largest magnitude is 0x7E = 448.
+ */
+double oracle_fp8_e4m3_to_double(uint8_t c) {
+    const int sign = (c >> 7) & 1;
+    const int expo = (c >> 3) & 0xf;
+    const int mant = c & 7;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant, -9);
+    else
+        v = ldexp((double)(8 + mant), expo - 10);
+    return sign ? -v : v;
+}
+
+/*
+ * Nearest E4M3 code to y, ties to the even code (the code's lowest bit is
+ * the mantissa's), magnitudes above 448 saturating to 448, NaN to 0x7F.
+ * Written as a search over the 127 non-negative finite codes, which are
+ * exact in double, so every comparison is exact.
+ */
+uint8_t oracle_fp8_e4m3_from_float(float y) {
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    const double a = fabs((double)y);
+    int best = 0;
+    double best_err = a;  /* code 0 is +0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double err = fabs(oracle_fp8_e4m3_to_double((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    if (a > 448.0) best = 0x7E;
+    return (uint8_t)(sign | best);
+}
+
+/* Quantisation of one fp16 value with scale s: the quotient x / s is formed
+ * in binary32 (IEEE division, rounded to nearest) and then encoded. */
+static uint8_t quantize_fp8(uint16_t xh, float s) {
+    const float x = (float)oracle_half_to_double(xh);
+    const float y = x / s;
+    return oracle_fp8_e4m3_from_float(y);
+}
+
+void oracle_fp8_quantize_array(uint8_t* dst, const uint16_t* src, int64_t n, float s) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = quantize_fp8(src[i], s);
+}
+
+/*
+ * Append into FP8 pools: as oracle_paged_append, with every element of head
+ * h of the new token stored as its quantisation with k_scale[h] (K) or
+ * v_scale[h] (V).  Pools: [num_blocks][block_size][kv_heads][head_dim] bytes.
+ */
+int oracle_paged_append_fp8(uint8_t* k_pool, uint8_t* v_pool, const float* k_scale,
+                            const float* v_scale, const int32_t* block_tables,
+                            const int32_t* positions, const uint16_t* k_new,
+                            const uint16_t* v_new, int rows, int kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_row, int num_blocks) {
+    if (rows < 0 || kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        const int pos = positions[r];
+        if (pos < 0) continue;
+        if (pos / block_size >= max_blocks_per_row) return ORACLE_BAD_TABLE;
+        const int32_t pb = block_tables[(int64_t)r * max_blocks_per_row + pos / block_size];
+        if (pb < 0 || pb >= num_blocks) return ORACLE_BAD_TABLE;
+    }
+    for (int r = 0; r < rows; ++r) {
+        const int pos = positions[r];
+        if (pos < 0) continue;
+        const int64_t pb = block_tables[(int64_t)r * max_blocks_per_row + pos / block_size];
+        for (int h = 0; h < kv_heads; ++h) {
+            const int64_t dst = idx4(pb, pos % block_size, h, 0, block_size, kv_heads, head_dim);
+            const int64_t src = ((int64_t)r * kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                k_pool[dst + d] = quantize_fp8(k_new[src + d], k_scale[h]);
+                v_pool[dst + d] = quantize_fp8(v_new[src + d], v_scale[h]);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Paged decode over FP8 pools: the definition of oracle_paged_decode with
+ * K_t[d] = e4m3(k code) * k_scale[kvh] and V_t[d] = e4m3(v code) *
+ * v_scale[kvh], all in double.
+ */
+int oracle_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_pool,
+                            const uint8_t* v_pool, const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, const int32_t* seq_lens, int rows,
+                            int q_heads, int kv_heads, int head_dim, int block_size,
+                            double scale, int max_blocks_per_row, int num_blocks,
+                            int num_threads) {
+    if (!check_heads(q_heads, kv_heads, head_dim) || block_size <= 0 || rows < 0)
+        return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        const int L = seq_lens[r];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks_per_row * block_size)
+            return ORACLE_BAD_ARG;
+        for (int lb = 0; lb < (L + block_size - 1) / block_size; ++lb) {
+            const int32_t pb = block_tables[(int64_t)r * max_blocks_per_row + lb];
+            if (pb < 0 || pb >= num_blocks) return ORACLE_BAD_TABLE;
+        }
+    }
+    const int group = q_heads / kv_heads;
+    int failed = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int r = 0; r < rows; ++r) {
+        for (int h = 0; h < q_heads; ++h) {
+            const int L = seq_lens[r];
+            const int kvh = h / group;
+            double* o = out + ((int64_t)r * q_heads + h) * head_dim;
+            const uint16_t* qv = q + ((int64_t)r * q_heads + h) * head_dim;
+            double* s = (double*)malloc(sizeof(double) * (L + 1));
+            if (!s) {
+#pragma omp atomic write
+                failed = 1;
+                continue;
+            }
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (L > 0) {
+                double m = -INFINITY;
+                for (int t = 0; t < L; ++t) {
+                    const int64_t pb = block_tables[(int64_t)r * max_blocks_per_row + t / block_size];
+                    const int64_t off = idx4(pb, t % block_size, kvh, 0, block_size, kv_heads, head_dim);
+                    double acc = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        acc += oracle_half_to_double(qv[d]) *
+                               (oracle_fp8_e4m3_to_double(k_pool[off + d]) * (double)k_scale[kvh]);
+                    s[t] = scale * acc;
+                    if (s[t] > m) m = s[t];
+                }
+                double z = 0.0;
+                for (int t = 0; t < L; ++t) {
+                    s[t] = exp(s[t] - m);
+                    z += s[t];
+                }
+                for (int t = 0; t < L; ++t) {
+                    const int64_t pb = block_tables[(int64_t)r * max_blocks_per_row + t / block_size];
+                    const int64_t off = idx4(pb, t % block_size, kvh, 0, block_size, kv_heads, head_dim);
+                    const double w = s[t] / z;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += w * (oracle_fp8_e4m3_to_double(v_pool[off + d]) * (double)v_scale[kvh]);
+                }
+            }
+            free(s);
+        }
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}

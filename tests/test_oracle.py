@@ -342,3 +342,112 @@ def test_prefill_scatter_then_gather_recovers_the_prompts():
         k, v = wl.logical_tokens(c2, 0, r)
         assert np.array_equal(k, ks[r, src_start[r]:].view(np.uint16))
         assert np.array_equal(v, vs[r, src_start[r]:].view(np.uint16))
+
+
+# --- FP8 (E4M3) pools ----------------------------------------------------------
+# The pages name FP8 KV without fixing a format ("PagedAttention", section
+# "Checking it on a real system"); the oracle takes OCP E4M3 with one scale
+# per KV head.  These pins tie it to the format's definition, to PyTorch's
+# independent float8_e4m3fn conversion, and to the fp16 oracle.
+
+def test_fp8_decode_matches_format_definition_values():
+    c = oracle.fp8_e4m3_to_double
+    expect = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+              0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0}
+    for code, v in expect.items():
+        assert c([code])[0] == v, hex(code)
+    assert np.isnan(c([0x7F, 0xFF])).all()
+    assert math.copysign(1.0, c([0x80])[0]) == -1.0
+    pos = c(np.arange(0x7F))
+    assert np.all(np.diff(pos) > 0)  # finite non-negative codes increase
+
+
+def test_fp8_decode_matches_torch_for_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    ours = oracle.fp8_e4m3_to_double(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_fp8_encode_rounds_to_nearest_even_and_saturates():
+    enc = oracle.fp8_e4m3_from_float
+    assert list(enc([1.0625, 1.1875, 1.03125])) == [0x38, 0x3A, 0x38]   # ties to even, below tie
+    assert list(enc([2.0 ** -10, 1.5 * 2.0 ** -10, 2.0 ** -11])) == [0x00, 0x01, 0x00]
+    assert list(enc([448.0, 449.0, 1000.0, -1e30])) == [0x7E, 0x7E, 0x7E, 0xFE]
+    assert list(enc([-0.0, 0.0])) == [0x80, 0x00]
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(enc(oracle.fp8_e4m3_to_double(finite).astype(np.float32)), finite)
+
+
+def test_fp8_encode_matches_torch_in_range():
+    torch = pytest.importorskip("torch")
+    g = torch.Generator().manual_seed(3)
+    y = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-12, 9, (20000,), generator=g).float())
+    y = y[y.abs() <= 448].float()
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.fp8_e4m3_from_float(y.numpy()), ref)
+
+
+def test_fp8_quantize_divides_in_binary32_first():
+    x = np.array([0.1, -3.0, 250.0, 1e-4], dtype=np.float16)
+    s = np.float32(0.37)
+    expect = oracle.fp8_e4m3_from_float(x.astype(np.float32) / s)
+    assert np.array_equal(oracle.fp8_quantize(x, s), expect)
+
+
+def test_fp8_append_writes_quantised_slots_only():
+    rng = np.random.default_rng(4)
+    nb, bs, hk, d, rows = 6, 16, 2, 8, 3
+    kp = rng.integers(0, 0x7E, (nb, bs, hk, d), dtype=np.uint8)
+    vp = rng.integers(0, 0x7E, (nb, bs, hk, d), dtype=np.uint8)
+    bt = np.array([[4, 1], [0, 5], [2, 3]], dtype=np.int32)
+    pos = np.array([17, 3, -1], dtype=np.int32)
+    kn = _f16(rng.standard_normal((rows, hk, d)))
+    vn = _f16(rng.standard_normal((rows, hk, d)))
+    ks = np.array([0.05, 0.2], dtype=np.float32)
+    vs = np.array([0.1, 0.01], dtype=np.float32)
+    k2, v2 = oracle.paged_append_fp8(kp, vp, ks, vs, bt, pos, kn, vn)
+    ek, ev = kp.copy(), vp.copy()
+    for r, (b, o) in enumerate([(1, 1), (0, 3)]):
+        for h in range(hk):
+            ek[b, o, h] = oracle.fp8_quantize(kn[r, h].view(np.float16), ks[h])
+            ev[b, o, h] = oracle.fp8_quantize(vn[r, h].view(np.float16), vs[h])
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+
+
+def test_fp8_decode_equals_fp16_decode_on_exactly_representable_pools():
+    # E4M3 values times a power-of-two scale are exact in fp16 (within its
+    # range), so the FP8 decode must equal the fp16 oracle on those values.
+    rng = np.random.default_rng(5)
+    lengths, bs, hq, hk, d = [1, 17, 40], 16, 4, 2, 8
+    case = _rand_case(9, lengths, bs, hq=hq, hk=hk, d=d, nan=False)
+    nb = case.k_pool[0].shape[0]
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F and (c & 0x78) >= 0x20], dtype=np.uint8)
+    kp8 = rng.choice(finite, (nb, bs, hk, d))
+    vp8 = rng.choice(finite, (nb, bs, hk, d))
+    ks = np.array([0.25, 2.0], dtype=np.float32)
+    vs = np.array([0.5, 0.125], dtype=np.float32)
+    kf = (oracle.fp8_e4m3_to_double(kp8) * ks[None, None, :, None]).astype(np.float16)
+    vf = (oracle.fp8_e4m3_to_double(vp8) * vs[None, None, :, None]).astype(np.float16)
+    assert np.array_equal(kf.astype(np.float64), oracle.fp8_e4m3_to_double(kp8) * ks[None, None, :, None])
+    a = oracle.paged_decode_fp8(case.q[0], kp8, vp8, ks, vs, case.block_tables, case.seq_lens, case.scale)
+    b = oracle.paged_decode(case.q[0], kf, vf, case.block_tables, case.seq_lens, case.scale)
+    assert np.max(np.abs(a - b)) <= 1e-12
+
+
+def test_fp8_decode_scales_output_with_v_scale():
+    rng = np.random.default_rng(6)
+    case = _rand_case(11, [5, 30], 16, hq=4, hk=2, d=8, nan=False)
+    nb = case.k_pool[0].shape[0]
+    kp8 = rng.integers(0x20, 0x60, (nb, 16, 2, 8), dtype=np.uint8)
+    vp8 = rng.integers(0x20, 0x60, (nb, 16, 2, 8), dtype=np.uint8)
+    ks = np.array([0.3, 0.7], dtype=np.float32)
+    a = oracle.paged_decode_fp8(case.q[0], kp8, vp8, ks, np.array([1.0, 1.0], np.float32),
+                                case.block_tables, case.seq_lens, case.scale)
+    b = oracle.paged_decode_fp8(case.q[0], kp8, vp8, ks, np.array([3.0, 0.5], np.float32),
+                                case.block_tables, case.seq_lens, case.scale)
+    assert np.allclose(b[:, :2], 3.0 * a[:, :2], rtol=1e-13, atol=0)
+    assert np.allclose(b[:, 2:], 0.5 * a[:, 2:], rtol=1e-13, atol=0)
