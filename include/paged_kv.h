@@ -244,6 +244,44 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
                                   float scale, void* workspace, size_t workspace_bytes,
                                   int32_t* dev_err, cudaStream_t stream);
 
+/*
+ * FP8 KV pools.  "PagedAttention" (deepconcepts.dev), section "Checking it on
+ * a real system", names FP8 KV as a way to change the bytes per token; the
+ * pages fix no format.  Here a pool holds E4M3 codes (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; no infinities, 0x7F / 0xFF are NaN, 448 is
+ * the largest value), laid out like the fp16 pools but one byte per element:
+ * [num_blocks][block_size][kv_heads][head_dim].  k_scale, v_scale: device
+ * float [kv_heads]; code c of head h stands for e4m3(c) * scale[h].
+ *
+ * paged_kv_append_fp8 -- paged_kv_append into FP8 pools: element x of head h
+ * of the new token is stored as the nearest E4M3 value of the binary32
+ * quotient x / scale[h], ties to even, magnitudes above 448 saturating to 448.
+ * Bit-exact; errors and skipped rows as in paged_kv_append.  The pools need
+ * 8-byte alignment, k_new / v_new 16-byte alignment; head_dim % 8 == 0.
+ */
+int paged_kv_append_fp8(void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, const int32_t* positions, const void* k_new,
+                        const void* v_new, int rows, int kv_heads, int head_dim, int block_size,
+                        int max_blocks_per_row, int num_blocks, int32_t* dev_err,
+                        cudaStream_t stream);
+
+/*
+ * paged_attention_decode_fp8 -- paged_attention_decode over FP8 pools: the
+ * same attention with K and V dequantised as e4m3(code) * scale[kv head].
+ * Arguments, workspace (paged_attention_workspace_size), errors and
+ * device-side checks as in paged_attention_decode.  Supported for head_dim
+ * 128, q_heads / kv_heads <= 8, kv_heads <= 16, block_size a multiple of 16
+ * and rows <= 1024 (PKV_ERR_UNSUPPORTED otherwise).  The scales are read once
+ * per launch.
+ */
+int paged_attention_decode_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, const int32_t* seq_lens, int rows,
+                               int q_heads, int kv_heads, int head_dim, int block_size, float scale,
+                               int max_blocks_per_row, int num_blocks, int max_seq_len,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                               cudaStream_t stream);
+
 /* Bytes of the static device scratch behind paged_attention_decode_noalloc
  * (8 MiB, held by every GPU that loads the library until the process exits). */
 #define PKV_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)

@@ -72,6 +72,7 @@ constexpr uint32_t kPollLimit = 1u << 21;  // polls of a merge wait (about a sec
 constexpr uint32_t kBoxBytes = kGranule * 128;   // 16 rows x 128 B (64 dims)
 constexpr uint32_t kSlotBytes = 4 * kBoxBytes;   // K dims 0-63, K 64-127, V 0-63, V 64-127
 constexpr uint32_t kSlotV = 2 * kBoxBytes;
+constexpr int kFp8MaxKvHeads = 16;                // FP8 pools: per-head scales kept in shared memory
 constexpr uint32_t kQBytes = 8 * 256;            // up to 8 query heads x 128 dims
 constexpr int kCombStride = 68;                  // stream combine: 64 dims + 4 pad (floats)
 constexpr int kDumpStride = 132;                 // burst dump: 128 dims + 4 pad (floats)
@@ -100,6 +101,9 @@ struct Params {
     const __half* v_new;
     __half* kpool;
     __half* vpool;
+    // FP8 pools: one scale per KV head (null for fp16 pools)
+    const float* k_scale;
+    const float* v_scale;
 };
 
 // Burst-mode plan of one block, written by thread 0 after the prologue.
@@ -121,7 +125,8 @@ struct Smem {
     static constexpr uint32_t desc = bars + (2 * kStages + kRing + 2) * 8;          // TileDesc[S]
     static constexpr uint32_t plan = desc + kStages * 64;
     static constexpr uint32_t flags = plan + ((sizeof(Plan) + 15) / 16) * 16;       // misc ints
-    static constexpr uint32_t ppos = flags + 16 * 4;                                // piece positions [32]
+    static constexpr uint32_t scales = flags + 16 * 4;                              // FP8: k, v scale [2][16]
+    static constexpr uint32_t ppos = scales + 2 * kFp8MaxKvHeads * 4;               // piece positions [32]
     static constexpr uint32_t part = comb;  // scan partials: prologue only, aliases comb
     static constexpr uint32_t prefix = ppos + kMaxPieces * 4;                       // rows + 1 ints
     __host__ __device__ static constexpr uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
@@ -388,6 +393,52 @@ __device__ __forceinline__ bool prepare_granule(unsigned char* slot_ptr, int val
     return wrote;
 }
 
+// FP8 pools: the producer lands a granule's E4M3 K box (16 tokens x 128
+// bytes, 128-byte swizzle) at +0 and its V box at +2 KB of the slot; the
+// owning warp widens both in place to the fp16 slot layout attend expects
+// (exact: every E4M3 value is an fp16 value; the per-head scales are applied
+// to the scores and to the output instead).  All of the warp's reads happen
+// before any of its writes.
+__device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
+    uint4 kc[4], vc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = lane + 32 * k, r = i >> 3, c = i & 7;
+        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+        kc[k] = *reinterpret_cast<const uint4*>(slot + off);
+        vc[k] = *reinterpret_cast<const uint4*>(slot + kBoxBytes + off);
+    }
+    __syncwarp();
+    auto widen = [](uint32_t w, uint32_t& lo, uint32_t& hi) {
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    };
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = lane + 32 * k, r = i >> 3, c = i & 7;
+        // 16 dims 16c..16c+15: fp16 chunks 2(c%4), 2(c%4)+1 of box c/4
+        const uint32_t j0 = (c & 3) * 2;
+        const uint32_t b0 = (c >> 2) * kBoxBytes + r * 128;
+        const uint32_t o0 = b0 + ((j0 ^ (r & 7)) << 4), o1 = b0 + (((j0 + 1) ^ (r & 7)) << 4);
+        uint4 a, b;
+        widen(kc[k].x, a.x, a.y);
+        widen(kc[k].y, a.z, a.w);
+        widen(kc[k].z, b.x, b.y);
+        widen(kc[k].w, b.z, b.w);
+        *reinterpret_cast<uint4*>(slot + o0) = a;
+        *reinterpret_cast<uint4*>(slot + o1) = b;
+        widen(vc[k].x, a.x, a.y);
+        widen(vc[k].y, a.z, a.w);
+        widen(vc[k].z, b.x, b.y);
+        widen(vc[k].w, b.z, b.w);
+        *reinterpret_cast<uint4*>(slot + kSlotV + o0) = a;
+        *reinterpret_cast<uint4*>(slot + kSlotV + o1) = b;
+    }
+    __syncwarp();
+}
+
 // Log-sum-exp merge of P partial records (children j = 0..P-1, rec_floats
 // apart) for head mh, dims md..md+7: M = max_j m_j, then
 // L = sum_j 2^(m_j - M) l_j and o = sum_j 2^(m_j - M) o_j, summed in child order
@@ -566,7 +617,7 @@ __device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int
     }
 }
 
-template <bool kPaged>
+template <bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_tma_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const Params p) {
@@ -588,6 +639,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
     int* sm_pre = reinterpret_cast<int*>(smem + Smem::prefix);
     int* sm_len = reinterpret_cast<int*>(smem + Smem::lens(p.rows));
+    float* sm_ks = reinterpret_cast<float*>(smem + Smem::scales);  // FP8 only
+    float* sm_vs = sm_ks + kFp8MaxKvHeads;
+    // bytes the producer lands per granule
+    constexpr uint32_t kGranuleLoad = kFp8 ? 2 * kBoxBytes : kSlotBytes;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -609,6 +664,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         sm_flags[0] = 0;  // abort
         sm_flags[3] = 0;  // split pieces recorded ([4..13]: their unit, first block, pieces, row, head)
     }
+    if (kFp8 && tid < 2 * p.hk) sm_ks[tid < p.hk ? tid : kFp8MaxKvHeads + tid - p.hk] =
+        tid < p.hk ? p.k_scale[tid] : p.v_scale[tid - p.hk];
 
     // ---- granule prefix over rows: sm_pre[r] = first granule of row r ----
     const int per = (rows + kThreads - 1) / kThreads;
@@ -721,13 +778,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 sm_plan->valid[lane] = valid;
                 const uint32_t fb = bar_slot + 8 * lane;
-                mbar_arrive_expect_tx(fb, issue ? kSlotBytes : 0u);
+                mbar_arrive_expect_tx(fb, issue ? kGranuleLoad : 0u);
                 if (issue) {
                     const uint32_t dst = sbase + Smem::ring + lane * kSlotBytes;
-                    tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
+                    if (kFp8) {
+                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kBoxBytes, &vmap, 0, kvh, zrow, fb);
+                    } else {
+                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
+                        tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
+                    }
                 }
             }
             griddep_wait();
@@ -837,15 +899,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, mine && issue));
                 __syncwarp();
                 const uint32_t fb = bar_full + 8 * s;
-                if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kSlotBytes + (first ? qbytes : 0u));
+                if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kGranuleLoad + (first ? qbytes : 0u));
                 __syncwarp();
                 if (mine && issue) {
                     const uint32_t dst =
                         sbase + Smem::ring + (s * kTileGranules + lane - j) * kSlotBytes;
-                    tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
+                    if (kFp8) {
+                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kBoxBytes, &vmap, 0, kvh, zrow, fb);
+                    } else {
+                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
+                        tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
+                        tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
+                    }
                 }
                 if (first && lane == 0 && waited)
                     bulk_load(sbase + Smem::q + s * kQBytes,
@@ -963,17 +1030,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slot[j] = sbase + Smem::ring + si * kSlotBytes;
                     valid[j] = pl.valid[si];
                     const int gtok = (bs + j - us) * kGranule;
+                    if (kFp8) {
+                        widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
+                        wrote = true;
+                    }
                     wrote |= prepare_granule(smem + Smem::ring + si * kSlotBytes, valid[j],
                                              patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
                 }
                 if (!ok) break;
                 if (wrote) __syncwarp();
+                const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
                 if (nb == 3)
-                    attend<3>(st, qb, slot, valid, p.scale_log2, lane);
+                    attend<3>(st, qb, slot, valid, sl2, lane);
                 else if (nb == 2)
-                    attend<2>(st, qb, slot, valid, p.scale_log2, lane);
+                    attend<2>(st, qb, slot, valid, sl2, lane);
                 else
-                    attend<1>(st, qb, slot, valid, p.scale_log2, lane);
+                    attend<1>(st, qb, slot, valid, sl2, lane);
             }
             // Dump the warp's state into its first slot: m[8], l[8], o[8][132].
             __syncwarp();
@@ -1048,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 const int r = pl.r[pc], kvh = pl.kvh[pc];
                 if (pl.P[pc] == 1) {
-                    const float inv = L > 0.f ? __fdividef(1.f, L) : 0.f;
+                    const float inv = L > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, L) : 0.f;
                     uint4 pk;
                     pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
                     pk.y = pack_half2(acc[2] * inv, acc[3] * inv);
@@ -1176,12 +1248,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (warp < ng) {
                 const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
                 const int si = s * kTileGranules + warp;
-                const bool wrote = prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
+                if (kFp8) widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
+                const bool wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
                                                    patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
                 if (wrote) __syncwarp();
                 const uint32_t slot[1] = {sbase + Smem::ring + si * kSlotBytes};
                 const int vv[1] = {valid};
-                attend<1>(st, qb, slot, vv, p.scale_log2, lane);
+                attend<1>(st, qb, slot, vv, kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2, lane);
                 // Generic-proxy writes must be ordered before TMA reuses the slot.
                 if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
@@ -1226,7 +1299,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 rec[ch] = Mh;
                 rec[8 + ch] = Lh;
             }
-            const float inv = Lh > 0.f ? __fdividef(1.f, Lh) : 0.f;
+            const float inv = Lh > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, Lh) : 0.f;
             const int cq = (tid & 15) * 4;  // four dims within a 64-dim pass
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
@@ -1373,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 merge_children<false>(land, P, p.rec_floats, mh, md, Ls, acc);
             else
                 merge_children<true>(glob, P, p.rec_floats, mh, md, Ls, acc);
-            const float iv = Ls > 0.f ? __fdividef(1.f, Ls) : 0.f;
+            const float iv = Ls > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, Ls) : 0.f;
             uint4 pk;
             pk.x = pack_half2(acc[0] * iv, acc[1] * iv);
             pk.y = pack_half2(acc[2] * iv, acc[3] * iv);
@@ -1411,20 +1484,25 @@ struct MapKey {
     const void* base;
     int64_t rows;
     int hk;
-    bool operator==(const MapKey& o) const { return base == o.base && rows == o.rows && hk == o.hk; }
+    bool fp8;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && hk == o.hk && fp8 == o.fp8;
+    }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
-        return std::hash<const void*>()(k.base) ^ (std::hash<int64_t>()(k.rows) * 31) ^ k.hk;
+        return std::hash<const void*>()(k.base) ^ (std::hash<int64_t>()(k.rows) * 31) ^ k.hk ^
+               (k.fp8 ? 0x9e3779b9u : 0u);
     }
 };
 
-// Tensor map over a pool viewed as [rows][hk][128] fp16: box 64 dims x 1 head
-// x 16 tokens, 128-byte swizzle.
-static int pool_map(const void* base, int64_t rows, int hk, CUtensorMap* out) {
+// Tensor map over a pool viewed as [rows][hk][128] elements, 128-byte swizzle:
+// fp16, box 64 dims x 1 head x 16 tokens; FP8 (bytes), box 128 dims x 1 head
+// x 16 tokens.  Either way a box row is 128 bytes.
+static int pool_map(const void* base, int64_t rows, int hk, bool fp8, CUtensorMap* out) {
     static std::mutex mu;
     static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{base, rows, hk};
+    const MapKey key{base, rows, hk, fp8};
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) {
@@ -1434,11 +1512,13 @@ static int pool_map(const void* base, int64_t rows, int hk, CUtensorMap* out) {
     EncodeFn enc = encode_fn();
     if (!enc) return PKV_ERR_CUDA;
     CUtensorMap m;
+    const cuuint64_t esize = fp8 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hk, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hk * kHeadDim * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kGranule};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * esize, (cuuint64_t)hk * kHeadDim * esize};
+    const cuuint32_t box[3] = {fp8 ? 128u : 64u, 1, (cuuint32_t)kGranule};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+    if (enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PKV_ERR_CUDA;
@@ -1450,7 +1530,7 @@ static int pool_map(const void* base, int64_t rows, int hk, CUtensorMap* out) {
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set[2] = {false, false};
+    bool attr_set[3] = {false, false, false};
 };
 
 static int device_info(DeviceInfo** out) {
@@ -1506,9 +1586,12 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
                       const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
                       int max_seq_len, int width, void* workspace, int32_t* dev_err,
-                      cudaStream_t stream, const AppendArgs* append, bool pdl) {
+                      cudaStream_t stream, const AppendArgs* append, bool pdl,
+                      const float* k_scale, const float* v_scale) {
     using namespace tma;
     const bool paged = width == 0;
+    const bool fp8 = k_scale != nullptr;
+    if (fp8 && (!paged || !v_scale || kv_heads > kFp8MaxKvHeads || append)) return PKV_ERR_UNSUPPORTED;
     const int64_t pool_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)rows * width;
     if (pool_rows >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
     const int limit = paged ? max_seq_len : width;
@@ -1519,8 +1602,8 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     int st = device_info(&info);
     if (st != PKV_OK) return st;
     CUtensorMap km, vm;
-    if ((st = pool_map(k_base, pool_rows, kv_heads, &km)) != PKV_OK) return st;
-    if ((st = pool_map(v_base, pool_rows, kv_heads, &vm)) != PKV_OK) return st;
+    if ((st = pool_map(k_base, pool_rows, kv_heads, fp8, &km)) != PKV_OK) return st;
+    if ((st = pool_map(v_base, pool_rows, kv_heads, fp8, &vm)) != PKV_OK) return st;
 
     int64_t ctas = info->sms;
     if (ctas > kMaxCtas) ctas = kMaxCtas;
@@ -1554,9 +1637,13 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
         prm.vpool = static_cast<__half*>(const_cast<void*>(v_base));
     }
 
+    prm.k_scale = k_scale;
+    prm.v_scale = v_scale;
+
     const uint32_t smem = Smem::total(rows);
-    const int which = paged ? 0 : 1;
-    auto kernel = paged ? decode_tma_kernel<true> : decode_tma_kernel<false>;
+    const int which = fp8 ? 2 : paged ? 0 : 1;
+    auto kernel = fp8 ? decode_tma_kernel<true, true>
+                      : paged ? decode_tma_kernel<true, false> : decode_tma_kernel<false, false>;
     if (!info->attr_set[which]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Smem::total(kMaxRows)) != cudaSuccess)

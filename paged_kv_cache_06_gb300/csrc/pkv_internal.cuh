@@ -55,6 +55,7 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
                       const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
                       int max_seq_len, int width, void* workspace, int32_t* dev_err,
-                      cudaStream_t stream, const AppendArgs* append = nullptr, bool pdl = false);
+                      cudaStream_t stream, const AppendArgs* append = nullptr, bool pdl = false,
+                      const float* k_scale = nullptr, const float* v_scale = nullptr);
 
 }  // namespace pkv

@@ -72,6 +72,11 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_append_decode.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I,
                                                 P, S, ctypes.c_uint, P, P]
     L.paged_attention_append_decode.restype = I
+    L.paged_kv_append_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    L.paged_kv_append_fp8.restype = I
+    L.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P,
+                                             S, P, P]
+    L.paged_attention_decode_fp8.restype = I
     L.paged_kv_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
     L.paged_kv_copy_blocks.restype = I
     L.paged_kv_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
@@ -163,6 +168,44 @@ def prefill_scatter(k_pool, v_pool, block_tables, src_start, dst_start, lengths,
                                         _ptr(v_src), rows, width, hk, d, bs, block_tables.shape[1],
                                         nb, _ptr(dev_err), _stream(stream))
     _check("paged_kv_prefill_scatter", st)
+
+
+def append_fp8(k_pool, v_pool, k_scale, v_scale, block_tables, positions, k_new, v_new,
+               dev_err=None, stream=None):
+    """paged_kv_append_fp8: quantise each row's new token into its FP8 slot."""
+    for t, n, dt, nd in ((k_pool, "k_pool", torch.uint8, 4), (v_pool, "v_pool", torch.uint8, 4),
+                         (k_scale, "k_scale", torch.float32, 1), (v_scale, "v_scale", torch.float32, 1),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (positions, "positions", torch.int32, 1),
+                         (k_new, "k_new", torch.float16, 3), (v_new, "v_new", torch.float16, 3)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    nb, bs, hk, d = k_pool.shape
+    st = lib().paged_kv_append_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(block_tables), _ptr(positions), _ptr(k_new), _ptr(v_new),
+                                   positions.shape[0], hk, d, bs, block_tables.shape[1], nb,
+                                   _ptr(dev_err), _stream(stream))
+    _check("paged_kv_append_fp8", st)
+
+
+def decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, scale: float,
+               max_seq_len: int, workspace, dev_err=None, stream=None):
+    """paged_attention_decode_fp8: attention over FP8 pools with per-head scales."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.uint8, 4), (v_pool, "v_pool", torch.uint8, 4),
+                         (k_scale, "k_scale", torch.float32, 1), (v_scale, "v_scale", torch.float32, 1),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(seq_lens), rows, hq, hk, d, bs, float(scale),
+        block_tables.shape[1], nb, int(max_seq_len), _ptr(workspace), workspace.numel(),
+        _ptr(dev_err), _stream(stream))
+    _check("paged_attention_decode_fp8", st)
 
 
 def workspace_size(rows: int, q_heads: int, kv_heads: int, head_dim: int, max_seq_len: int,

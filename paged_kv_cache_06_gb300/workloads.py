@@ -99,6 +99,18 @@ def _randn_fp16(gen: torch.Generator, shape) -> np.ndarray:
     return t.numpy().view(np.uint16)
 
 
+def fp8_codes(gen: torch.Generator, shape) -> np.ndarray:
+    """Seeded random E4M3 codes for FP8 pools: a random sign bit, exponent
+    field uniform in 3..10 and mantissa field uniform in 0..7, so that with a
+    scale near 1/8 the stored values have magnitudes like N(0, 1) draws.
+    Pure bit assembly: no quantisation happens here."""
+    shape = tuple(shape)
+    sign = torch.randint(0, 2, shape, generator=gen, dtype=torch.int32)
+    expo = torch.randint(3, 11, shape, generator=gen, dtype=torch.int32)
+    mant = torch.randint(0, 8, shape, generator=gen, dtype=torch.int32)
+    return ((sign << 7) | (expo << 3) | mant).to(torch.uint8).numpy()
+
+
 def _assign_tables(lengths: np.ndarray, block_size: int, perm: np.ndarray,
                    max_blocks_per_row: int, shared_ids: Optional[np.ndarray] = None
                    ) -> np.ndarray:
