@@ -95,6 +95,8 @@ def _load():
             lib.oracle_paged_append_fp8.restype = I
             lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, I, I]
             lib.oracle_paged_decode_fp8.restype = I
+            lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, I, I, I]
+            lib.oracle_paged_prefill.restype = I
             _lib = lib
     return _lib
 
@@ -292,4 +294,28 @@ def paged_decode_fp8(q, k_pool8, v_pool8, k_scale, v_scale, block_tables, seq_le
                                          _ptr(bt), _ptr(sl), rows, hq, hk, d, bs, float(scale),
                                          bt.shape[1], nb, int(num_threads))
     _check(rc, "paged_decode_fp8")
+    return out
+
+
+# --- chunked prefill: several queries per row, causal within the chunk ----------
+
+def paged_prefill(q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: float,
+                  num_threads: int = 1) -> np.ndarray:
+    """fp64 causal attention of each row's chunk of newest tokens.
+
+    q: [total][Hq][D] (rows' chunks packed in order, q_start[r]..q_start[r+1]);
+    query i of row r sits at position seq_lens[r] - chunk + i and attends to
+    the row's tokens 0..that position.  Returns [total][Hq][D] float64.
+    """
+    q = _bits(q); kp = _bits(k_pool); vp = _bits(v_pool)
+    bt = _i32(block_tables); sl = _i32(seq_lens); qs = _i32(q_start)
+    total, hq, d = q.shape
+    nb, bs, hk, d2 = kp.shape
+    rows = sl.shape[0]
+    assert d2 == d and qs.shape == (rows + 1,) and int(qs[-1]) == total
+    out = np.zeros((total, hq, d), dtype=np.float64)
+    rc = _load().oracle_paged_prefill(_ptr(out), _ptr(q), _ptr(kp), _ptr(vp), _ptr(bt), _ptr(sl),
+                                      _ptr(qs), rows, hq, hk, d, bs, float(scale), bt.shape[1], nb,
+                                      int(num_threads))
+    _check(rc, "paged_prefill")
     return out

@@ -66,3 +66,22 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, scale):
             row_out.append(o)
         out.append(row_out)
     return out
+
+
+def paged_prefill(q, k_pool, v_pool, block_tables, seq_lens, q_start, scale):
+    """Causal chunk attention, brute force: q nested [total][Hq][D] bits.
+
+    For each query the visible tokens are gathered block by block, the
+    softmax is taken without max subtraction and summed in reverse order,
+    as in paged_decode above."""
+    out = []
+    rows = len(seq_lens)
+    for r in range(rows):
+        lo, hi = int(q_start[r]), int(q_start[r + 1])
+        C = hi - lo
+        for i in range(C):
+            pos = int(seq_lens[r]) - C + i
+            # a decode of this single query over tokens 0..pos
+            out.append(paged_decode([q[lo + i]], k_pool, v_pool, [block_tables[r]], [pos + 1],
+                                    scale)[0])
+    return out

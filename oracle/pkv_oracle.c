@@ -576,3 +576,73 @@ int oracle_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_poo
     }
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
+
+/*
+ * Chunked prefill: several query tokens per row, causal within the chunk.
+ * "Paged attention" (danielfleming.xyz), section "What changed" and the
+ * closing paragraphs: the next engine splits long prompts into fixed chunks
+ * (512 tokens) so decode steps run between them; "Continuous batching", the
+ * closing section: split a long prefill into fixed size chunks.  Reading
+ * taken (the pages give no kernel): row r's chunk holds the
+ * C_r = q_start[r+1] - q_start[r] newest tokens of the row, at positions
+ * p_r + i with p_r = seq_lens[r] - C_r (their K/V already in the row's
+ * blocks); query i attends to the row's tokens 0 .. p_r + i (causal), with
+ * the same head grouping as decode.
+ *
+ * q: [q_start[rows]][q_heads][head_dim] fp16 bits (rows' chunks packed in
+ * order); out: the same shape, double.
+ */
+int oracle_paged_prefill(double* out, const uint16_t* q, const uint16_t* k_pool,
+                         const uint16_t* v_pool, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int32_t* q_start, int rows, int q_heads,
+                         int kv_heads, int head_dim, int block_size, double scale,
+                         int max_blocks_per_row, int num_blocks, int num_threads) {
+    if (!check_heads(q_heads, kv_heads, head_dim) || block_size <= 0 || rows < 0)
+        return ORACLE_BAD_ARG;
+    if (q_start[0] != 0) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        const int C = q_start[r + 1] - q_start[r];
+        const int L = seq_lens[r];
+        if (C < 0 || L < C || (int64_t)L > (int64_t)max_blocks_per_row * block_size)
+            return ORACLE_BAD_ARG;
+        for (int lb = 0; lb < (L + block_size - 1) / block_size; ++lb) {
+            const int32_t pb = block_tables[(int64_t)r * max_blocks_per_row + lb];
+            if (pb < 0 || pb >= num_blocks) return ORACLE_BAD_TABLE;
+        }
+    }
+    const int group = q_heads / kv_heads;
+    const int total = q_start[rows];
+    int failed = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int qi = 0; qi < total; ++qi) {
+        for (int h = 0; h < q_heads; ++h) {
+            int r = 0;
+            while (q_start[r + 1] <= qi) ++r;  /* row of packed query qi */
+            const int C = q_start[r + 1] - q_start[r];
+            const int pos = seq_lens[r] - C + (qi - q_start[r]);
+            const int n = pos + 1;  /* tokens 0 .. pos */
+            const int kvh = h / group;
+            const uint16_t** kp = (const uint16_t**)malloc(sizeof(void*) * (n + 1));
+            const uint16_t** vp = (const uint16_t**)malloc(sizeof(void*) * (n + 1));
+            double* s = (double*)malloc(sizeof(double) * (n + 1));
+            if (!kp || !vp || !s) {
+#pragma omp atomic write
+                failed = 1;
+            } else {
+                for (int t = 0; t < n; ++t) {
+                    const int64_t pb = block_tables[(int64_t)r * max_blocks_per_row + t / block_size];
+                    const int64_t off = idx4(pb, t % block_size, kvh, 0, block_size, kv_heads, head_dim);
+                    kp[t] = k_pool + off;
+                    vp[t] = v_pool + off;
+                }
+                attend_one(out + ((int64_t)qi * q_heads + h) * head_dim,
+                           q + ((int64_t)qi * q_heads + h) * head_dim, kp, vp, n, head_dim, scale, s);
+            }
+            free(kp);
+            free(vp);
+            free(s);
+        }
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}

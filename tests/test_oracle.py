@@ -451,3 +451,66 @@ def test_fp8_decode_scales_output_with_v_scale():
                                 case.block_tables, case.seq_lens, case.scale)
     assert np.allclose(b[:, :2], 3.0 * a[:, :2], rtol=1e-13, atol=0)
     assert np.allclose(b[:, 2:], 0.5 * a[:, 2:], rtol=1e-13, atol=0)
+
+
+# --- chunked prefill (several queries per row, causal within the chunk) ---------
+
+def _prefill_case(seed, lengths, chunks, bs, hq=4, hk=2, d=8):
+    c = _rand_case(seed, lengths, bs, hq=hq, hk=hk, d=d, nan=True)
+    rng = np.random.default_rng(seed)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = _f16(rng.standard_normal((int(qs[-1]), hq, d)))
+    return c, q, qs
+
+
+@pytest.mark.parametrize("seed,lengths,chunks,bs", [
+    (1, [5, 9], [5, 3], 4), (2, [7, 1, 12], [2, 1, 12], 4), (3, [20], [7], 8)])
+def test_prefill_matches_pure_python_brute_force(seed, lengths, chunks, bs):
+    c, q, qs = _prefill_case(seed, lengths, chunks, bs)
+    ours = oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs, c.scale)
+    ref = np.array(brute.paged_prefill(q.tolist(), c.k_pool[0].tolist(), c.v_pool[0].tolist(),
+                                       c.block_tables.tolist(), c.seq_lens.tolist(), qs.tolist(),
+                                       c.scale)).reshape(ours.shape)
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_chunk_of_one_is_decode():
+    c, q, qs = _prefill_case(4, [1, 17, 40], [1, 1, 1], 16)
+    ours = oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs, c.scale)
+    dec = oracle.paged_decode(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    np.testing.assert_allclose(ours, dec, rtol=0, atol=0)
+
+
+def test_prefill_whole_prompt_is_causal_self_attention():
+    # A chunk that is the whole prompt: masked softmax(q k^T) v over the
+    # gathered tokens, computed with dense matrix products.
+    L, bs, hq, hk, d = 37, 8, 4, 2, 8
+    c, q, qs = _prefill_case(5, [L], [L], bs, hq, hk, d)
+    ours = oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs, c.scale)
+    K = np.empty((L, hk, d)); V = np.empty((L, hk, d))
+    for t in range(L):
+        pb = c.block_tables[0, t // bs]
+        K[t] = oracle.half_to_double(c.k_pool[0][pb, t % bs])
+        V[t] = oracle.half_to_double(c.v_pool[0][pb, t % bs])
+    Q = oracle.half_to_double(q)
+    mask = np.tril(np.ones((L, L), dtype=bool))
+    for h in range(hq):
+        kvh = h // (hq // hk)
+        s = c.scale * Q[:, h, :] @ K[:, kvh, :].T
+        s = np.where(mask, s, -np.inf)
+        p = scipy.special.softmax(s, axis=1)
+        np.testing.assert_allclose(ours[:, h, :], p @ V[:, kvh, :], rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_last_query_equals_decode_of_the_row():
+    c, q, qs = _prefill_case(6, [33, 64, 9], [8, 16, 9], 16)
+    ours = oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs, c.scale)
+    last = q[qs[1:] - 1]
+    dec = oracle.paged_decode(last, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, c.scale)
+    np.testing.assert_allclose(ours[qs[1:] - 1], dec, rtol=0, atol=0)
+
+
+def test_prefill_rejects_chunk_longer_than_row():
+    c, q, qs = _prefill_case(7, [4, 6], [5, 1], 4)
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs, c.scale)
