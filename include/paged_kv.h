@@ -245,6 +245,33 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
                                   int32_t* dev_err, cudaStream_t stream);
 
 /*
+ * paged_attention_prefill -- chunked prefill: attention of several query
+ * tokens per row, causal within the row's chunk.  Defining passages:
+ * "Paged attention" (danielfleming.xyz), closing sections (long prompts split
+ * into fixed chunks, 512 tokens, so decode steps interleave) and
+ * "PagedAttention" (deepconcepts.dev), section "PagedAttention" (keys gathered
+ * through the row's block table).
+ *
+ * q: fp16 [total_q][q_heads][head_dim], the rows' chunks packed in order;
+ * q_start: device int32 [rows + 1], q_start[0] = 0, row r's queries are
+ * q_start[r] .. q_start[r+1]-1 (C_r of them, possibly 0).  seq_lens[r] counts
+ * the row's tokens including its chunk, whose K/V must already be in the
+ * row's blocks (paged_kv_append / paged_kv_prefill_scatter); query i of the
+ * chunk sits at position seq_lens[r] - C_r + i and attends to the row's
+ * tokens 0 .. that position.  out: fp16, the shape of q.  total_q = q_start[rows]
+ * (host value, sizes the launch).  A row with C_r > seq_lens[r] or
+ * seq_lens[r] > max_seq_len is skipped (its outputs untouched) and flagged
+ * PKV_DEV_ERR_SEQ_LEN; table entries as in paged_attention_decode.  Supported
+ * for head_dim 128, block_size a multiple of 16, rows <= 1024.  No workspace.
+ */
+int paged_attention_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* q_start, int rows, int total_q, int q_heads,
+                            int kv_heads, int head_dim, int block_size, float scale,
+                            int max_blocks_per_row, int num_blocks, int max_seq_len,
+                            int32_t* dev_err, cudaStream_t stream);
+
+/*
  * FP8 KV pools.  "PagedAttention" (deepconcepts.dev), section "Checking it on
  * a real system", names FP8 KV as a way to change the bytes per token; the
  * pages fix no format.  Here a pool holds E4M3 codes (1 sign, 4 exponent bits

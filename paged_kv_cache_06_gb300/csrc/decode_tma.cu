@@ -46,9 +46,9 @@
 #include <cuda.h>
 
 #include <mutex>
-#include <unordered_map>
 
 #include "pkv_internal.cuh"
+#include "ptx.cuh"
 
 namespace pkv {
 namespace tma {
@@ -76,7 +76,6 @@ constexpr int kFp8MaxKvHeads = 16;                // FP8 pools: per-head scales 
 constexpr uint32_t kQBytes = 8 * 256;            // up to 8 query heads x 128 dims
 constexpr int kCombStride = 68;                  // stream combine: 64 dims + 4 pad (floats)
 constexpr int kDumpStride = 132;                 // burst dump: 128 dims + 4 pad (floats)
-constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
 static_assert(kSlotBytes % 1024 == 0, "slots must keep 1024-byte alignment for 128B swizzle");
@@ -137,92 +136,12 @@ struct Smem {
 static_assert(Smem::total(32) + 1024 <= 233472 / 2, "two blocks per SM at 32 rows");
 
 // ---------------------------------------------------------------------------
-// PTX wrappers
+// PTX wrappers (shared ones in ptx.cuh)
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait by a whole warp: every lane polls and a vote decides, so the
-// warp leaves together (true) or gives up together after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    return false;
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                        uint32_t& a3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                          uint32_t& a3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
+using namespace ptx;
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0).
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Stream-mode tile descriptor: written by the producer before the stage's
@@ -254,10 +173,6 @@ __device__ __forceinline__ int owner_of(int g, int W, int G) {
     return c;
 }
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Running softmax state of one warp: per lane, heads 2tq and 2tq+1
 // (tq = lane & 3) and the O^T fragments of all eight 16-dim row groups.
@@ -1461,71 +1376,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------------------------------
 // Host side
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeFn encode_fn() {
-    static EncodeFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(f);
-    });
-    return fn;
-}
-
-struct MapKey {
-    const void* base;
-    int64_t rows;
-    int hk;
-    bool fp8;
-    bool operator==(const MapKey& o) const {
-        return base == o.base && rows == o.rows && hk == o.hk && fp8 == o.fp8;
-    }
-};
-struct MapKeyHash {
-    size_t operator()(const MapKey& k) const {
-        return std::hash<const void*>()(k.base) ^ (std::hash<int64_t>()(k.rows) * 31) ^ k.hk ^
-               (k.fp8 ? 0x9e3779b9u : 0u);
-    }
-};
-
 // Tensor map over a pool viewed as [rows][hk][128] elements, 128-byte swizzle:
 // fp16, box 64 dims x 1 head x 16 tokens; FP8 (bytes), box 128 dims x 1 head
 // x 16 tokens.  Either way a box row is 128 bytes.
 static int pool_map(const void* base, int64_t rows, int hk, bool fp8, CUtensorMap* out) {
-    static std::mutex mu;
-    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{base, rows, hk, fp8};
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-        *out = it->second;
-        return PKV_OK;
-    }
-    EncodeFn enc = encode_fn();
-    if (!enc) return PKV_ERR_CUDA;
-    CUtensorMap m;
-    const cuuint64_t esize = fp8 ? 1 : 2;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hk, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * esize, (cuuint64_t)hk * kHeadDim * esize};
-    const cuuint32_t box[3] = {fp8 ? 128u : 64u, 1, (cuuint32_t)kGranule};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-            const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PKV_ERR_CUDA;
-    if (cache.size() > 4096) cache.clear();
-    cache.emplace(key, m);
-    *out = m;
-    return PKV_OK;
+    const int64_t esize = fp8 ? 1 : 2;
+    const int64_t dims[3] = {kHeadDim, hk, rows};
+    const int64_t strides[2] = {kHeadDim * esize, hk * kHeadDim * esize};
+    const int box[3] = {fp8 ? 128 : 64, 1, kGranule};
+    return tiled_map_3d(base, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        dims, strides, box, out);
 }
 
 struct DeviceInfo {

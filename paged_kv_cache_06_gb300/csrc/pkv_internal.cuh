@@ -1,6 +1,7 @@
 // Internal helpers shared by libpagedkv's CUDA translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -51,6 +52,11 @@ struct AppendArgs {
     const void* k_new;
     const void* v_new;
 };
+// Cached tiled tensor map (128-byte swizzle) over a 3-D array: dims and box
+// innermost first, strides in bytes of dims 1 and 2.
+int tiled_map_3d(const void* base, CUtensorMapDataType dtype, const int64_t dims[3],
+                 const int64_t strides[2], const int box[3], CUtensorMap* out);
+
 int tma_decode_launch(void* out, const void* q, const void* k_base, const void* v_base,
                       const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,

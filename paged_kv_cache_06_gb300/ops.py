@@ -77,6 +77,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P,
                                              S, P, P]
     L.paged_attention_decode_fp8.restype = I
+    L.paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P]
+    L.paged_attention_prefill.restype = I
     L.paged_kv_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
     L.paged_kv_copy_blocks.restype = I
     L.paged_kv_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
@@ -206,6 +208,27 @@ def decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
         block_tables.shape[1], nb, int(max_seq_len), _ptr(workspace), workspace.numel(),
         _ptr(dev_err), _stream(stream))
     _check("paged_attention_decode_fp8", st)
+
+
+def prefill(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: float,
+            max_seq_len: int, dev_err=None, stream=None):
+    """paged_attention_prefill: causal attention of each row's chunk of new tokens."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1), (q_start, "q_start", torch.int32, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    total, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    rows = seq_lens.shape[0]
+    if q_start.shape[0] != rows + 1:
+        raise ValueError("q_start must have rows + 1 entries")
+    st = lib().paged_attention_prefill(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(q_start), rows, total, hq, hk, d, bs, float(scale), block_tables.shape[1], nb,
+        int(max_seq_len), _ptr(dev_err), _stream(stream))
+    _check("paged_attention_prefill", st)
 
 
 def workspace_size(rows: int, q_heads: int, kv_heads: int, head_dim: int, max_seq_len: int,

@@ -1,0 +1,99 @@
+"""GPU parity for chunked-prefill paged attention (causal within each chunk).
+
+|gpu - oracle| <= 2e-3 + 2e-3 * |oracle| elementwise, as for decode.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_06_gb300 import ops
+from paged_kv_cache_06_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 2e-3
+
+
+def assert_close(gpu, ref, what=""):
+    g = gpu.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g)), what
+    err = np.abs(g - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        pytest.fail(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at {i}: "
+                    f"gpu {g[i]} oracle {ref[i]}")
+
+
+def prefill_case(lengths, chunks, bs, seed):
+    case = wl.custom(lengths, bs, seed=seed, append=False, nan_fill=True, extra_blocks=2)
+    gen = torch.Generator().manual_seed(seed + 500)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = wl._randn_fp16(gen, (int(qs[-1]), case.q_heads, case.head_dim))
+    return case, q, qs
+
+
+def run(case, q, qs, dev_err=None, tables=None):
+    d = wl.to_device(case)
+    bt = d["block_tables"] if tables is None else torch.from_numpy(tables).cuda()
+    gq = torch.from_numpy(q.view(np.int16)).view(torch.float16).cuda()
+    out = torch.full(gq.shape, float("nan"), dtype=torch.float16, device="cuda")
+    ops.prefill(out, gq, d["k_pool"][0], d["v_pool"][0], bt, d["seq_lens"],
+                torch.from_numpy(qs).cuda(), case.scale, case.max_seq_len, dev_err=dev_err)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("lengths,chunks,bs", [
+    ([100], [100], 16),                      # whole prompt, ragged last tile
+    ([64, 300, 16], [17, 130, 16], 16),      # chunks at the end of longer rows
+    ([1, 65, 200, 5], [1, 64, 65, 0], 64),   # a row with no queries
+    ([640], [512], 32),                      # one 512-token chunk after 128 cached tokens
+])
+def test_prefill_matches_oracle(cuda_device, lengths, chunks, bs):
+    case, q, qs = prefill_case(lengths, chunks, bs, seed=sum(chunks) + bs)
+    ref = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables, case.seq_lens,
+                               qs, case.scale, num_threads=oracle.default_threads())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(case, q, qs, dev_err=err)
+    assert int(err.item()) == 0
+    assert_close(out, ref, f"prefill {lengths} {chunks}")
+
+
+def test_prefill_512_chunks_on_4096_rows_sampled(cuda_device):
+    """Two rows of 4096 tokens whose last 512 form the chunk (block size 64):
+    every query of the first and last 64-query tile, and a sample between."""
+    case, q, qs = prefill_case([4096, 4096], [512, 512], 64, seed=11)
+    out = run(case, q, qs)
+    idx = np.r_[0:64, 448:576, 960:1024, 200:201, 700:701]
+    ref_all = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables,
+                                   case.seq_lens, qs, case.scale, num_threads=oracle.default_threads())
+    assert_close(out[torch.from_numpy(idx)], ref_all[idx], "512-token chunks")
+
+
+def test_prefill_bit_identical_under_block_permutation(cuda_device):
+    case, q, qs = prefill_case([300, 77], [120, 77], 16, seed=13)
+    out1 = run(case, q, qs)
+    # move every block to a new physical id
+    nb = case.num_blocks
+    perm = np.random.default_rng(1).permutation(nb).astype(np.int32)
+    kp = np.empty_like(case.k_pool[0]); vp = np.empty_like(case.v_pool[0])
+    kp[perm] = case.k_pool[0]; vp[perm] = case.v_pool[0]
+    bt = np.where(case.block_tables >= 0, perm[np.maximum(case.block_tables, 0)], -1).astype(np.int32)
+    case2 = wl.DecodeCase(**{**case.__dict__, "k_pool": kp[None], "v_pool": vp[None],
+                             "block_tables": bt})
+    out2 = run(case2, q, qs)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_prefill_bad_chunk_is_flagged_and_skipped(cuda_device):
+    case, q, qs = prefill_case([10, 40], [12, 8], 16, seed=14)  # row 0: chunk longer than the row
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(case, q, qs, dev_err=err)
+    assert int(err.item()) & 2
+    ref = oracle.paged_prefill(q[12:], case.k_pool[0], case.v_pool[0], case.block_tables[1:],
+                               case.seq_lens[1:], qs[1:] - 12, case.scale)
+    assert_close(out[12:], ref, "the valid row")
+    assert torch.isnan(out[:12].float()).all()  # skipped row untouched
