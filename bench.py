@@ -172,6 +172,20 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def load_tensor_peak():
+    """Dense fp16/bf16 tensor peak: the measured cuBLAS bf16 burst figure (the
+    fp16 rate is the same on this part), else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        v = m.get("bf16_tflops")
+        if v:
+            return float(v), "measured (bf16 burst)"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback"
+
+
 def decode_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_06_gb300", "csrc")
@@ -353,6 +367,29 @@ def run_ours(args, rank, world, pg):
     g8 = capture(step_fp8)
     ms8, _ = time_graph(g8, args.steps, args.warmup)
     del g8, kp8, vp8
+
+    # Chunked prefill: 8 rows whose newest 512 tokens (the pages' chunk size)
+    # are the chunk, at 4096 tokens of context, one layer's pool.
+    pcase = wl.custom([4096] * 8, 64, seed=args.seed + 3, layers=1, append=False, nan_fill=False)
+    pd = wl.to_device(pcase, dev)
+    pchunk = 512
+    pqs = torch.arange(0, pchunk * (pcase.rows + 1), pchunk, dtype=torch.int32, device=dev)
+    pgen = torch.Generator().manual_seed(args.seed + 4)
+    pq = torch.randn(pcase.rows * pchunk, hq, hd, generator=pgen).to(torch.float16).to(dev)
+    pout = torch.empty_like(pq)
+
+    def step_prefill():
+        ops.prefill(pout, pq, pd["k_pool"][0], pd["v_pool"][0], pd["block_tables"],
+                    pd["seq_lens"], pqs, pcase.scale, pcase.max_seq_len)
+
+    g_pf = capture(step_prefill)
+    ms_pf, _ = time_graph(g_pf, args.steps, args.warmup)
+    del g_pf
+    # causal FLOPs: query i of a chunk sees (context - chunk + i + 1) keys;
+    # 2 flops per multiply-add, QK^T and PV, every query head
+    vis = sum(4096 - pchunk + i + 1 for i in range(pchunk))
+    pf_flops = pcase.rows * hq * vis * hd * 2 * 2
+    tf_peak, tf_kind = load_tensor_peak()
     n_app = int((case.positions >= 0).sum())
     bytes8 = (b["kv_logical"] // 2 + b["q_out"] + b["table"]
               + n_app * hk * hd * (2 + 1) * 2)  # append: fp16 in, one byte out, K and V
@@ -379,6 +416,15 @@ def run_ours(args, rank, world, pg):
         "decode_only": {"ms_per_step": round(ms_dec, 5),
                         "us_per_launch": round(ms_dec * 1e3 / L, 3),
                         "GBps": round(b["decode_layer"] / (ms_dec * 1e-3 / L) / 1e9, 2)},
+        "prefill": {"what": "paged_attention_prefill, 8 rows x 512-token chunk at 4096 context, "
+                            "12 query / 2 KV heads, mma.sync fp16 in / fp32 accumulate",
+                    "ms_per_launch": round(ms_pf, 5),
+                    "prompt_tokens_per_s": round(pcase.rows * pchunk / (ms_pf * 1e-3), 1),
+                    "roofline": {"bound": "tensor",
+                                 "achieved": round(pf_flops / (ms_pf * 1e-3) / 1e12, 2),
+                                 "peak": tf_peak, "unit": "TFLOP/s",
+                                 "frac": round(pf_flops / (ms_pf * 1e-3) / 1e12 / tf_peak, 4),
+                                 "peak_source": tf_kind, "flops_per_launch": pf_flops}},
         "fp8_step": {"ms_per_step": round(ms8, 5),
                      "value": round(L * bytes8 / (ms8 * 1e-3) / 1e9, 2), "unit": "GB/s",
                      "bytes_per_layer": bytes8,
