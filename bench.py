@@ -190,7 +190,8 @@ def decode_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_06_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("decode") and name.endswith((".cu", ".cuh")):
+        if (name.startswith("decode") and name.endswith((".cu", ".cuh"))) or \
+                name in ("ptx.cuh", "pkv_internal.cuh", "tmap.cu"):
             h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
