@@ -28,8 +28,8 @@
 //   * burst: the block's whole range fits the ring and covers at most four
 //     pieces.  Every copy is issued before the dependency wait, warps are
 //     dealt to pieces in proportion to their size, and each warp attends to
-//     its granules (up to three at once) in one pass; the warps' partial
-//     states are then combined for all pieces together.
+//     its granules; the warps' partial states are then combined for all
+//     pieces together.
 //   * stream: the ring runs as three stages of four granules, one granule
 //     per warp per stage, and pieces are combined as they end.
 // Per granule (16 tokens) and group of query heads (up to 8):
@@ -66,7 +66,7 @@ constexpr int kRecHead = 16;   // per record: m[8], l[8], then o[group][128]
 constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
 constexpr int kMergeBatch = 8; // children merged per register batch
 constexpr int kBurstPieces = 4;
-constexpr int kBatch = 3;      // burst mode: granules attended together by one warp
+constexpr int kBatch = 1;      // burst mode: granules per attend step (larger batches measured slower)
 constexpr int kCounterStride = 32;  // ints between the arrival counters of two units
 constexpr uint32_t kPollLimit = 1u << 21;  // polls of a merge wait (about a second)
 constexpr uint32_t kBoxBytes = kGranule * 128;   // 16 rows x 128 B (64 dims)
@@ -955,12 +955,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!ok) break;
                 if (wrote) __syncwarp();
                 const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
-                if (nb == 3)
-                    attend<3>(st, qb, slot, valid, sl2, lane);
-                else if (nb == 2)
-                    attend<2>(st, qb, slot, valid, sl2, lane);
-                else
-                    attend<1>(st, qb, slot, valid, sl2, lane);
+                attend<1>(st, qb, slot, valid, sl2, lane);
             }
             // Dump the warp's state into its first slot: m[8], l[8], o[8][132].
             __syncwarp();
@@ -1269,20 +1264,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
-    // ---- split pieces: every piece's record is published; the block that
-    // holds a unit's last piece waits for the others and merges the unit
-    // through the log-sum-exp of all its records (a block holds the last
-    // piece of at most one split unit: its first piece) ----
+    // ---- split pieces.  Every piece publishes its record and counts itself
+    // on the unit's counter with a release.  The block holding the unit's
+    // last piece waits (bounded) until all P pieces have counted, lands their
+    // records and combines them through their log-sum-exp, then re-arms the
+    // counter.  A block merges at most one unit: the one whose end is its
+    // first piece.  (Splitting a long unit's merge over several blocks, one
+    // query head each, measured slower.) ----
     // Shared memory written through the generic proxy (partials, patches) is
-    // ordered before the bulk copies that may land records over it.
+    // ordered before the bulk copies that may land records over it, and the
+    // records written here before the bulk copies that may read them back.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     consumer_sync();
     const int nsplit = sm_flags[3];
     if (nsplit == 0 || sm_flags[0]) return;
-    // Records written here through the generic proxy may be read back by the
-    // bulk copies of the landing below.
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    consumer_sync();
     if (tid < nsplit) {
         // The barrier above orders every thread's record stores before this
         // thread's release.
@@ -1290,21 +1286,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int cs = sm_flags[5 + 5 * tid];
         const int P = sm_flags[6 + 5 * tid];
         int* ctr = p.counters + (int64_t)u * kCounterStride;
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
         int merge = 0;
-        if (cta != cs + P - 1) {
-            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
-        } else {
-            // Bounded wait for the other P - 1 pieces; the acquire makes their
-            // records visible to this block after the next barrier.
+        if (cta == cs + P - 1) {
+            // the acquire makes every piece's record visible to this block
+            // after the next barrier
             int seen = 0;
             for (uint32_t i = 0; i < kPollLimit; ++i) {
                 asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
-                if (seen >= P - 1) break;
+                if (seen >= P) break;
                 __nanosleep(32);
             }
-            if (seen >= P - 1) {
-                // with the relaxed read that saw every release, this fence
-                // makes the pieces' records visible
+            if (seen >= P) {
                 *ctr = 0;  // every piece has arrived: re-arm for the next call
                 merge = 1;
             } else {
@@ -1316,30 +1309,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     consumer_sync();
     if (sm_flags[0]) return;
-    const uint32_t rec_bytes = (uint32_t)p.rec_floats * 4u;
-    uint32_t land_total = 0;
+    int job = -1;
     for (int k = 0; k < nsplit; ++k)
-        if (sm_flags[14 + k]) land_total += (uint32_t)sm_flags[6 + 5 * k] * rec_bytes;
-    if (land_total == 0) return;
-    // The ring is idle once the block's granules are consumed: every child
-    // record of the units merged here comes in by bulk copies at once.
+        if (sm_flags[14 + k]) job = k;
+    if (job < 0) return;
+    const int u = sm_flags[4 + 5 * job], cs = sm_flags[5 + 5 * job], P = sm_flags[6 + 5 * job];
+    const int r = sm_flags[7 + 5 * job], kvh = sm_flags[8 + 5 * job];
+    const float vs = kFp8 ? sm_vs[kvh] : 1.f;
+    const uint32_t rec_bytes = (uint32_t)p.rec_floats * 4u;
     // The ring is idle once the block's granules are consumed: the records
-    // of the merged unit land there by bulk copies issued at once.
-    const bool landing = land_total <= (uint32_t)(kRing * kSlotBytes);
+    // land there by bulk copies issued at once.
+    const bool landing = (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
     if (landing) {
         if (warp == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            if (lane == 0) mbar_arrive_expect_tx(bar_merge, land_total);
+            if (lane == 0) mbar_arrive_expect_tx(bar_merge, (uint32_t)P * rec_bytes);
             __syncwarp();
-            uint32_t off = 0;
-            for (int k = 0; k < nsplit; ++k) {
-                if (!sm_flags[14 + k]) continue;
-                const int u = sm_flags[4 + 5 * k], cs = sm_flags[5 + 5 * k], P = sm_flags[6 + 5 * k];
-                for (int j = lane; j < P; j += 32)
-                    bulk_load(sbase + Smem::ring + off + j * rec_bytes,
-                              p.records + (int64_t)(cs + j + u) * p.rec_floats, rec_bytes, bar_merge);
-                off += (uint32_t)P * rec_bytes;
-            }
+            for (int j = lane; j < P; j += 32)
+                bulk_load(sbase + Smem::ring + j * rec_bytes,
+                          p.records + (int64_t)(cs + j + u) * p.rec_floats, rec_bytes, bar_merge);
         }
         if (!mbar_wait(bar_merge, 0)) {
             if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
@@ -1348,28 +1335,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int mh = tid >> 4;        // head
     const int md = (tid & 15) * 8;  // eight dims
-    uint32_t off = 0;
-    for (int k = 0; k < nsplit; ++k) {
-        if (!sm_flags[14 + k]) continue;
-        const int u = sm_flags[4 + 5 * k], cs = sm_flags[5 + 5 * k], P = sm_flags[6 + 5 * k];
-        const int r = sm_flags[7 + 5 * k], kvh = sm_flags[8 + 5 * k];
-        if (mh < p.group) {
-            float Ls = 0.f, acc[8];
-            const float* land = reinterpret_cast<const float*>(smem + Smem::ring + off);
-            const float* glob = p.records + (int64_t)(cs + u) * p.rec_floats;
-            if (landing)
-                merge_children<false>(land, P, p.rec_floats, mh, md, Ls, acc);
-            else
-                merge_children<true>(glob, P, p.rec_floats, mh, md, Ls, acc);
-            const float iv = Ls > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, Ls) : 0.f;
-            uint4 pk;
-            pk.x = pack_half2(acc[0] * iv, acc[1] * iv);
-            pk.y = pack_half2(acc[2] * iv, acc[3] * iv);
-            pk.z = pack_half2(acc[4] * iv, acc[5] * iv);
-            pk.w = pack_half2(acc[6] * iv, acc[7] * iv);
-            *reinterpret_cast<uint4*>(p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim + md) = pk;
-        }
-        off += (uint32_t)P * rec_bytes;
+    if (mh < p.group) {
+        float Ls = 0.f, acc[8];
+        if (landing)
+            merge_children<false>(reinterpret_cast<const float*>(smem + Smem::ring), P, p.rec_floats,
+                                  mh, md, Ls, acc);
+        else
+            merge_children<true>(p.records + (int64_t)(cs + u) * p.rec_floats, P, p.rec_floats, mh,
+                                 md, Ls, acc);
+        const float iv = Ls > 0.f ? __fdividef(vs, Ls) : 0.f;
+        uint4 pk;
+        pk.x = pack_half2(acc[0] * iv, acc[1] * iv);
+        pk.y = pack_half2(acc[2] * iv, acc[3] * iv);
+        pk.z = pack_half2(acc[4] * iv, acc[5] * iv);
+        pk.w = pack_half2(acc[6] * iv, acc[7] * iv);
+        *reinterpret_cast<uint4*>(p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim + md) = pk;
     }
 }
 
