@@ -568,6 +568,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int rows = p.rows;
 
 
+    if (warp == kConsumerWarps && lane == 0) {
+        // fetch the tensor-map descriptors now; the first copy would wait for them
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
@@ -648,9 +653,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int Geff = W < G ? W : G;
     const int g0 = cta < Geff ? (int)((int64_t)W * cta / Geff) : 0;
     const int g1 = cta < Geff ? (int)((int64_t)W * (cta + 1) / Geff) : 0;
-    if (tid == 0) make_plan(*sm_plan, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
-    __syncthreads();
-    const bool burst = sm_plan->burst != 0;
 
     if (warp == kConsumerWarps) {
         // ============================ producer ============================
@@ -658,6 +660,26 @@ __global__ void __launch_bounds__(kThreads, 2)
             griddep_wait();
             if (kPaged) row_work(p, sm_pre, cta, G, lane);
             return;
+        }
+        // Burst mode when the range fits the ring and covers at most
+        // kBurstPieces units (the consumers' plan, made concurrently, takes
+        // the same decision).
+        bool burst = false;
+        if (g1 - g0 <= kRing) {
+            int u = -1;
+            if (lane < g1 - g0) {
+                const int gg = g0 + lane;
+                int lo = 0, hi = rows - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
+                }
+                const int n = (sm_pre[lo + 1] - sm_pre[lo]) / hk;
+                u = lo * hk + (gg - sm_pre[lo]) / n;
+            }
+            const int up = __shfl_up_sync(0xffffffffu, u, 1);
+            const int pieces = __popc(__ballot_sync(0xffffffffu, u >= 0 && (lane == 0 || u != up)));
+            burst = pieces <= kBurstPieces;
         }
         if (burst) {
             // Every granule of the range goes to its own slot now, before the
@@ -863,6 +885,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ============================== consumers ==============================
+    if (tid == 0) make_plan(*sm_plan, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
+    consumer_sync();
+    const bool burst = sm_plan->burst != 0;
     if (burst && sm_plan->wpiece[warp] >= 0) {
         // Warm L2 with this warp's query rows and new token.  A prefetch reads
         // nothing into the block, so it may precede the dependency wait: the
