@@ -418,7 +418,7 @@ def run_ours(args, rank, world, pg):
                         "us_per_launch": round(ms_dec * 1e3 / L, 3),
                         "GBps": round(b["decode_layer"] / (ms_dec * 1e-3 / L) / 1e9, 2)},
         "prefill": {"what": "paged_attention_prefill, 8 rows x 512-token chunk at 4096 context, "
-                            "12 query / 2 KV heads, mma.sync fp16 in / fp32 accumulate",
+                            "12 query / 2 KV heads, tcgen05 fp16 in / fp32 accumulate in TMEM",
                     "ms_per_launch": round(ms_pf, 5),
                     "prompt_tokens_per_s": round(pcase.rows * pchunk / (ms_pf * 1e-3), 1),
                     "roofline": {"bound": "tensor",
