@@ -1,5 +1,5 @@
 // Chunked-prefill paged attention on the 5th-generation tensor cores
-// (tcgen05, accumulators in tensor memory), sm_103a.
+// (tcgen05, accumulators and the probabilities in tensor memory), sm_103a.
 //
 // What it computes is paged_attention_prefill's definition ("Paged
 // attention", danielfleming.xyz, closing sections: long prompts split into
@@ -8,18 +8,31 @@
 // query i of row r's chunk sits at position seq_lens[r] - C_r + i and attends
 // causally to the row's tokens 0 .. that position.
 //
-// A block takes 128 queries of one row and one query head.  Warp roles:
-//   warps 0-3  softmax: thread i owns query row i, which is also TMEM lane i;
-//   warp 4     TMA: the queries once, then 64-token K/V tiles (four 16-token
-//              granules gathered through the block table) into a 3-stage ring;
-//   warp 5     MMA: one thread issues tcgen05.mma, f16 in / f32 accumulate:
-//                S_j[128 q][64 tok]  = Q[128][128] . K_j^T   (TMEM, double-buffered)
-//                O[128 q][128 dims] += P_j[128][64] . V_j    (TMEM)
-//              and commits each group to an mbarrier.
-// Per tile a softmax thread reads its S row from TMEM, applies the causal
-// mask, updates its running maximum and sum, rescales its O row in TMEM when
-// the maximum moved, and writes its fp16 P row (128-byte swizzled) to shared
-// memory for the PV product.  All waits are bounded.
+// A block takes 128 queries of one row and one query head and walks the
+// row's keys in 128-token tiles.  Warp roles:
+//   warps 0-7  softmax: warps w and w + 4 share query rows 32 (w % 4) .. (TMEM
+//              lanes); warp half hf = w / 4 takes tokens 64 hf .. 64 hf + 63 of
+//              each tile and head dims 64 hf .. 64 hf + 63 of Q and the output;
+//   warp 8     TMA: K tiles into a 4-slot ring;
+//   warp 9     TMA: V in 64-token halves into a 5-slot ring;
+//              each copy moves one box of 16, 32, 64 or 128 consecutive
+//              tokens of one page (the largest that divides the page size),
+//              its pool rows found through the block table;
+//   warp 10    S issue: S_t[128 q][128 tok] = Q . K_t^T, Q read from TMEM;
+//   warp 11    PV issue: O[128 q][128 dims] += P_t . V_t, P read from TMEM.
+// One thread of each issuing warp drives tcgen05.mma (f16 in, f32
+// accumulate) and commits each group to an mbarrier.  The queries are
+// copied into TMEM once; S is double-buffered in TMEM and each softmax half
+// stores its fp16 probabilities over the first half of its own S columns, so
+// S_{t+2} reuses a buffer only after PV_t has read P_t.  Per tile a softmax
+// thread reads its half S row, applies the causal mask, agrees on the row
+// maximum with its partner warp, rescales its half O row in TMEM when the
+// maximum moved, and stores its P.  Shared memory holds only K and V, which
+// leaves its bandwidth to the copies and the B operands.  The producer and
+// issuer loops keep slots, parities and descriptors as running values: each
+// of those warps runs alone, so its loop is a chain of dependent
+// instructions.  Every wait sleeps in mbarrier.try_wait and is bounded in
+// wall time.
 #include "pkv_internal.cuh"
 #include "ptx.cuh"
 
@@ -29,42 +42,50 @@ namespace prefill_tc {
 using namespace ptx;
 
 constexpr int kQTile = 128;
-constexpr int kKTile = 64;
-constexpr int kGranule = 16;
-constexpr int kStages = 3;
-constexpr int kSoftWarps = 4;
-constexpr int kThreads = (kSoftWarps + 2) * 32;  // softmax, TMA, MMA
+constexpr int kKTile = 128;
+constexpr int kGranule = 16;  // the k-step of the PV product and the smallest copy box
+constexpr int kKSlots = 4;     // K ring, 128 tokens a slot; free once its S product is done
+constexpr int kVSlots = 5;     // V ring, 64 tokens a slot; free once its PV product is done
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = (kSoftWarps + 4) * 32;  // softmax, K TMA, V TMA, S issue, PV issue
 constexpr int kMaxRows = 1024;
-constexpr uint32_t kHalfQ = kQTile * 128;         // 128 queries x 64 dims
-constexpr uint32_t kHalfKV = kKTile * 128;        // 64 tokens x 64 dims
-constexpr uint32_t kStageBytes = 4 * kHalfKV;     // K lo, K hi, V lo, V hi
-constexpr uint32_t kBox = kGranule * 128;         // one granule box
-constexpr uint32_t kTmemCols = 256;               // S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kKHalf = kKTile * 128;        // 128 tokens x 64 dims
+constexpr uint32_t kKSlot = 2 * kKHalf;          // K lo, K hi
+constexpr uint32_t kVHalf = 64 * 128;            // 64 tokens x 64 dims
+constexpr uint32_t kVSlot = 2 * kVHalf;          // V lo, V hi
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // S buffers [0, 128), [128, 256); P over [0, 32) and [64, 96) of each
+constexpr uint32_t kColO = 256;  // O [256, 384)
+constexpr uint32_t kColQ = 384;  // Q [384, 448): fp16 pairs of head dims
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
+    const __half* q;
     __half* out;
     const int32_t* tables;
     const int32_t* seq_lens;
     const int32_t* q_start;
     int rows, hq, group, bs, mbpr, nb, limit;
+    int kbox, vbox;  // tokens per K and V copy
     float scale_log2;
     int32_t* dev_err;
 };
 
 struct Smem {
-    static constexpr uint32_t q = 0;                                 // Q lo, Q hi
-    static constexpr uint32_t kv = q + 2 * kHalfQ;                   // [stages]
-    static constexpr uint32_t pbuf = kv + kStages * kStageBytes;     // P [2][128][64] fp16
-    static constexpr uint32_t bars = pbuf + 2 * kQTile * 128;        // q, full[3], empty[3], s[2], p[2], o[2]
-    static constexpr uint32_t tmem = bars + 16 * 8;                  // allocated TMEM address
-    static constexpr uint32_t part = tmem + 16;                      // scan partials [threads]
-    static constexpr uint32_t pre = part + kThreads * 4;             // tile prefix [rows + 1]
-    __host__ __device__ static constexpr uint32_t total(int rows) {
-        return pre + (uint32_t)(rows + 1) * 4 + 1024;
-    }
+    static constexpr uint32_t kring = 0;                           // [K slots]
+    static constexpr uint32_t vring = kring + kKSlots * kKSlot;    // [V slots]
+    static constexpr uint32_t bars = vring + kVSlots * kVSlot;     // 28 mbarriers
+    static constexpr uint32_t tmem = bars + 32 * 8;                // allocated TMEM address
+    static constexpr uint32_t xch = tmem + 16;                     // row maxima [2][2][128], sums [2][128]
+    // The tile scan's scratch (partials [threads], prefix [rows + 1]) lives
+    // in the K ring: it is read before the first copy is issued.
+    static constexpr uint32_t part = kring;
+    static constexpr uint32_t pre = part + kThreads * 4;
+    __host__ __device__ static constexpr uint32_t total() { return xch + 6 * kQTile * 4 + 1024; }
 };
-static_assert(Smem::kv % 1024 == 0 && Smem::pbuf % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(Smem::kring % 1024 == 0 && Smem::vring % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(Smem::pre + (kMaxRows + 1) * 4 <= Smem::kring + kKSlots * kKSlot, "scan scratch fits the K ring");
+static_assert(Smem::total() <= 232448, "shared memory per block");
 
 // Shared-memory matrix descriptor: 128-byte swizzle, version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -76,12 +97,21 @@ __device__ __forceinline__ uint32_t idesc(int M, int N, int b_mn_major) {
     return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                     uint32_t accumulate) {
+// D (TMEM) (+)= A (shared memory) . B (shared memory)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+// D (TMEM) (+)= A (TMEM: row m in lane m, column c holds k = 2c, 2c + 1) . B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -94,18 +124,26 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// 32 consecutive columns of this warp's 32 lanes.
+// Columns c .. c + 31 of this warp's 32 lanes; the wait is part of the same
+// statement, so no use of v can be scheduled before the data has arrived.
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(addr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(addr)
+        : "memory");
+}
+// Columns c .. c + 63: two loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, uint32_t (&v)[32], uint32_t (&w)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+          "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15]), "=r"(w[16]), "=r"(w[17]), "=r"(w[18]), "=r"(w[19]), "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]), "=r"(w[25]), "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+        : "r"(addr), "r"(addr + 32)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -117,23 +155,68 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&v)[32]
         "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
         "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Waits that sleep: try_wait with a suspend-time hint parks the thread
+// until the phase completes (or the hint runs out) instead of spinning, so a
+// waiting warp leaves the issue slots to the warps that share its
+// scheduler.  Each wait gives up after kWaitLimitNs of wall time.
+constexpr uint32_t kSuspendNs = 1000000;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+// One thread's bounded wait (the issuing threads wait alone).
+__device__ __forceinline__ bool mbar_wait1(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    while (now_ns() - t0 < kWaitLimitNs)
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+    return false;
+}
+// The whole warp waits and leaves together (true) or gives up together.
+__device__ __forceinline__ bool mbar_waitw(uint32_t bar, uint32_t parity) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
+    const uint64_t t0 = __shfl_sync(0xffffffffu, now_ns(), 0);
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
+        const bool late = __shfl_sync(0xffffffffu, now_ns(), 0) - t0 >= kWaitLimitNs;
+        if (late) return false;
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap kmap,
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_q = sbase + Smem::bars;
-    const uint32_t bar_full = bar_q + 8;                 // [3]
-    const uint32_t bar_empty = bar_full + kStages * 8;   // [3]
-    const uint32_t bar_s = bar_empty + kStages * 8;      // [2]
-    const uint32_t bar_p = bar_s + 16;  // [2]: P buffer b written (tiles b, b + 2, ...)
+    const uint32_t bar_q = sbase + Smem::bars;               // Q copied into TMEM
+    const uint32_t bar_kfull = bar_q + 8;                    // [K slots]
+    const uint32_t bar_kempty = bar_kfull + kKSlots * 8;     // [K slots]
+    const uint32_t bar_vfull = bar_kempty + kKSlots * 8;     // [V slots]
+    const uint32_t bar_vempty = bar_vfull + kVSlots * 8;     // [V slots]
+    const uint32_t bar_s = bar_vempty + kVSlots * 8;  // [2]: S buffer b computed (tiles b, b + 2, ...)
+    const uint32_t bar_p = bar_s + 16;  // [2]: P of S buffer b written
     const uint32_t bar_o = bar_p + 16;  // [2]: PV product of P buffer b done
+    const uint32_t bar_x = bar_o + 16;  // [2]: both halves' row maxima of a tile written
+    const uint32_t bar_l = bar_x + 16;  // both halves' row sums written
     uint32_t* sm_tmem = reinterpret_cast<uint32_t*>(smem + Smem::tmem);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
     int* sm_pre = reinterpret_cast<int*>(smem + Smem::pre);
@@ -214,16 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nq = min(kQTile, C - i_first);
     const int kend = pos0 + i_first + nq;  // keys 0 .. kend-1 are visible to someone
     const int nkt = (kend + kKTile - 1) / kKTile;
+    const int nvh = (kend + 63) / 64;      // 64-token V halves
     const int qrow0 = p.q_start[r] + i_first;
 
-    // ---- barriers and tensor memory ----
+    // ---- barriers and tensor memory (the scan scratch is dead from here) ----
     if (tid == 0) {
-        mbar_init(bar_q, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+        mbar_init(bar_q, kSoftWarps);
+        for (int s = 0; s < kKSlots; ++s) {
+            mbar_init(bar_kfull + 8 * s, 1);
+            mbar_init(bar_kempty + 8 * s, 1);
         }
+        for (int s = 0; s < kVSlots; ++s) {
+            mbar_init(bar_vfull + 8 * s, 1);
+            mbar_init(bar_vempty + 8 * s, 1);
+        }
+        mbar_init(bar_l, kSoftWarps);
         for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(bar_x + 8 * b2, kSoftWarps);
             mbar_init(bar_s + 8 * b2, 1);
             mbar_init(bar_p + 8 * b2, kSoftWarps);
             mbar_init(bar_o + 8 * b2, 1);
@@ -240,136 +330,241 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sm_tmem;
-    const uint32_t t_o = tmem + 128;  // O columns
 
-    if (warp == kSoftWarps) {
+    if (warp == kSoftWarps || warp == kSoftWarps + 1) {
         // ============================== TMA ==============================
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar_q, 2 * kHalfQ);
-            tma_load_3d(sbase + Smem::q, &qmap, 0, h, qrow0, bar_q);
-            tma_load_3d(sbase + Smem::q + kHalfQ, &qmap, 64, h, qrow0, bar_q);
-        }
-        for (int kt = 0; kt < nkt; ++kt) {
-            const int s = kt % kStages;
-            if (!mbar_wait(bar_empty + 8 * s, (((uint32_t)kt / kStages) & 1) ^ 1)) {
+        // Warp kSoftWarps streams K tiles, the next warp V halves; each
+        // granule's pool rows come from the block table.
+        const bool is_v = warp == kSoftWarps + 1;
+        const int nslots = is_v ? kVSlots : kKSlots;
+        const int nunits = is_v ? nvh : nkt;
+        const int unit_tok = is_v ? 64 : kKTile;
+        const uint32_t full0 = is_v ? bar_vfull : bar_kfull;
+        const uint32_t empty0 = is_v ? bar_vempty : bar_kempty;
+        const uint32_t ring = sbase + (is_v ? Smem::vring : Smem::kring);
+        const uint32_t slot_bytes = is_v ? kVSlot : kKSlot;
+        const uint32_t half_bytes = is_v ? kVHalf : kKHalf;
+        const CUtensorMap* map = is_v ? &vmap : &kmap;
+        // Block-table entries are fetched a batch ahead: lane l handles box
+        // l % gpu of unit l / gpu of a batch of 32 / gpu units, so the
+        // table's latency is paid once per batch and hidden behind the
+        // previous one.  Slots, parities and addresses advance by increments:
+        // this warp runs alone, and its loop is a chain of dependent
+        // instructions.
+        const int box = is_v ? p.vbox : p.kbox;
+        const int gpu = unit_tok / box;        // boxes per unit
+        const int upb = 32 / gpu;              // units per batch
+        const int my_j = lane / gpu, my_g = lane % gpu;
+        const uint32_t box_bytes = (uint32_t)box * 128;
+        auto fetch = [&](int ub) -> int {  // raw block id of this lane's box in the batch at unit ub
+            const int tok0 = (ub + my_j) * unit_tok + my_g * box;
+            return tok0 < kend ? __ldg(p.tables + (int64_t)r * p.mbpr + tok0 / p.bs) : 0;
+        };
+        auto to_row = [&](int ub, int pb) -> int {  // its pool row, or -1 for no copy
+            const int tok0 = (ub + my_j) * unit_tok + my_g * box;
+            if (tok0 >= kend) return -1;
+            if (pb < 0 || pb >= p.nb) {
+                flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+                return -1;
+            }
+            return pb * p.bs + tok0 % p.bs;
+        };
+        int pb_next = fetch(0);
+        int row = to_row(0, pb_next);
+        pb_next = fetch(upb);
+        int s = 0, j = 0;
+        uint32_t ph = 0, fb = full0, eb = empty0, slot = ring;
+        for (int u = 0; u < nunits; ++u) {
+            if (!mbar_waitw(eb, ph ^ 1)) {
                 if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
                 break;
             }
-            int zrow = 0;
-            bool issue = false;
-            if (lane < 4) {
-                const int tok0 = kt * kKTile + lane * kGranule;
-                if (tok0 < kend) {
-                    const int pb = p.tables[(int64_t)r * p.mbpr + tok0 / p.bs];
-                    if (pb < 0 || pb >= p.nb) {
-                        flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-                    } else {
-                        zrow = pb * p.bs + tok0 % p.bs;
-                        issue = true;
-                    }
-                }
-            }
+            const bool issue = my_j == j && row >= 0;
             const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, issue));
-            const uint32_t fb = bar_full + 8 * s;
-            if (lane == 0) mbar_arrive_expect_tx(fb, nissue * 4 * kBox);
+            if (lane == 0) mbar_arrive_expect_tx(fb, nissue * 2 * box_bytes);
             __syncwarp();
             if (issue) {
-                const uint32_t st = sbase + Smem::kv + s * kStageBytes + lane * kBox;
-                tma_load_3d(st, &kmap, 0, kvh, zrow, fb);
-                tma_load_3d(st + kHalfKV, &kmap, 64, kvh, zrow, fb);
-                tma_load_3d(st + 2 * kHalfKV, &vmap, 0, kvh, zrow, fb);
-                tma_load_3d(st + 3 * kHalfKV, &vmap, 64, kvh, zrow, fb);
+                const uint32_t st = slot + my_g * box_bytes;
+                tma_load_3d(st, map, 0, kvh, row, fb);
+                tma_load_3d(st + half_bytes, map, 64, kvh, row, fb);
+            }
+            if (++j == upb) {
+                j = 0;
+                row = to_row(u + 1, pb_next);
+                pb_next = fetch(u + 1 + upb);
+            }
+            if (++s == nslots) {
+                s = 0;
+                ph ^= 1;
+                fb = full0;
+                eb = empty0;
+                slot = ring;
+            } else {
+                fb += 8;
+                eb += 8;
+                slot += slot_bytes;
             }
         }
-    } else if (warp == kSoftWarps + 1) {
-        // ============================== MMA ==============================
-        const uint32_t id_s = idesc(kQTile, kKTile, 0);
-        const uint32_t id_o = idesc(kQTile, 128, 1);
-        bool ok = mbar_wait(bar_q, 0);
-        for (int kt = 0; ok && kt <= nkt; ++kt) {
-            if (kt < nkt) {
-                const int s = kt % kStages;
-                if (!(ok = mbar_wait(bar_full + 8 * s, ((uint32_t)kt / kStages) & 1))) break;
-                unsigned char* stp = smem + Smem::kv + s * kStageBytes;
-                // V rows past the last visible key may hold anything (or be
-                // unloaded): zero them so that 0 * V stays 0 in the PV product.
-                const int vrow0 = kend - kt * kKTile;
-                if (vrow0 < kKTile) {
-                    for (int i = lane; i < (kKTile - vrow0) * 16; i += 32) {
-                        const int row = vrow0 + (i >> 4), c = i & 15;
-                        *reinterpret_cast<uint4*>(stp + 2 * kHalfKV + (c >> 3) * kHalfKV + row * 128 +
+        // every armed slot's copies have landed before the block exits
+        for (int u = max(0, nunits - nslots); u < nunits; ++u)
+            if (!mbar_waitw(full0 + 8 * (u % nslots), (uint32_t)(u / nslots) & 1) && lane == 0)
+                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+    } else if (warp == kSoftWarps + 2) {
+        // ============================ S issue ============================
+        // S_t = Q . K_t^T into S buffer t & 1, once K_t has landed and
+        // PV_{t-2} has read P_{t-2} out of that buffer.
+        if (lane == 0) {
+            const uint32_t id_s = idesc(kQTile, kKTile, 0);
+            const uint64_t kd0 = sdesc(sbase + Smem::kring, 16, 1024);
+            uint64_t kd = kd0;
+            uint32_t kf = bar_kfull, ke = bar_kempty, ph = 0;
+            int s = 0;
+            bool ok = mbar_wait1(bar_q, 0);
+            for (int t = 0; ok && t < nkt; ++t) {
+                if (!(ok = mbar_wait1(kf, ph))) break;
+                if (t >= 2 && !(ok = mbar_wait1(bar_o + 8 * (t & 1), (((uint32_t)t >> 1) & 1) ^ 1))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + kColS + (t & 1) * kKTile;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_ts(d, tmem + kColQ + ks * 8,
+                            kd + (uint64_t)((((ks >> 2) * kKHalf) + (ks & 3) * 32) >> 4), id_s, ks > 0);
+                umma_commit(bar_s + 8 * (t & 1));
+                umma_commit(ke);  // K_t is no longer read
+                if (++s == kKSlots) {
+                    s = 0;
+                    ph ^= 1;
+                    kd = kd0;
+                    kf = bar_kfull;
+                    ke = bar_kempty;
+                } else {
+                    kd += kKSlot >> 4;
+                    kf += 8;
+                    ke += 8;
+                }
+            }
+            if (!ok) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+        }
+    } else if (warp == kSoftWarps + 3) {
+        // ============================ PV issue ===========================
+        // O += P_kt . V_kt once both V halves have landed and the softmax
+        // has stored P_kt; k-steps past the last visible key are skipped and
+        // rows of the last granule past it are zeroed (0 * V must stay 0
+        // whatever the pool holds there).
+        if (lane == 0) {
+            const uint32_t id_o = idesc(kQTile, 128, 1);
+            const uint64_t vd0 = sdesc(sbase + Smem::vring, kVHalf, 1024);
+            int va = 0;        // V slot of half 2 kt
+            uint32_t vph = 0;  // its fill parity
+            bool ok = true;
+            for (int kt = 0; ok && kt < nkt; ++kt) {
+                int vb = va + 1;
+                uint32_t vphb = vph;
+                if (vb == kVSlots) {
+                    vb = 0;
+                    vphb ^= 1;
+                }
+                const bool two = 2 * kt + 1 < nvh;
+                const int vrows = min(kKTile, kend - kt * kKTile);
+                const int nsteps = (vrows + 15) / 16;
+                if (!(ok = mbar_wait1(bar_vfull + 8 * va, vph))) break;
+                if (two && !(ok = mbar_wait1(bar_vfull + 8 * vb, vphb))) break;
+                if (vrows < nsteps * 16) {
+                    const int zr0 = vrows, zn = nsteps * 16 - vrows;
+                    unsigned char* vs = smem + Smem::vring + (zr0 >= 64 ? vb : va) * kVSlot;
+                    for (int i = 0; i < zn * 16; ++i) {
+                        const int row = (zr0 & 63) + (i >> 4), c = i & 15;
+                        *reinterpret_cast<uint4*>(vs + (c >> 3) * kVHalf + row * 128 +
                                                   (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
                 }
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t st = sbase + Smem::kv + s * kStageBytes;
-                    const uint32_t d = tmem + (kt & 1) * kKTile;
+                const int pb = kt & 1;
+                if (!(ok = mbar_wait1(bar_p + 8 * pb, ((uint32_t)kt >> 1) & 1))) break;
+                tc_fence_after();
+                const uint32_t pa = tmem + kColS + pb * kKTile;
+                const uint64_t da = vd0 + (uint64_t)(va * (kVSlot >> 4));
+                const uint64_t db = vd0 + (uint64_t)(vb * (kVSlot >> 4));
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = sdesc(sbase + Smem::q + (ks >> 2) * kHalfQ + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bk = sdesc(st + (ks >> 2) * kHalfKV + (ks & 3) * 32, 16, 1024);
-                        umma(d, a, bk, id_s, ks > 0);
-                    }
-                    umma_commit(bar_s + 8 * (kt & 1));
+                for (int kk = 0; kk < 8; ++kk) {
+                    // tokens 64 e .. 64 e + 63 sit in columns 64 e .. 64 e + 31
+                    if (kk < nsteps)
+                        umma_ts(tmem + kColO, pa + (kk >> 2) * 64 + (kk & 3) * 8,
+                                (kk < 4 ? da : db) + (uint64_t)((kk & 3) * 128), id_o,
+                                (kt > 0 || kk > 0) ? 1u : 0u);
                 }
-                __syncwarp();
-            }
-            if (kt > 0) {
-                // O += P_{kt-1} . V_{kt-1} once the softmax has written P_{kt-1}
-                const int j = kt - 1, s = j % kStages, pb = j & 1;
-                if (!(ok = mbar_wait(bar_p + 8 * pb, ((uint32_t)j >> 1) & 1))) break;
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t vb = sbase + Smem::kv + s * kStageBytes + 2 * kHalfKV;
-                    const uint32_t pa = sbase + Smem::pbuf + pb * (kQTile * 128);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc(pa + kk * 32, 16, 1024);
-                        const uint64_t bv = sdesc(vb + kk * 2048, kHalfKV, 1024);
-                        umma(t_o, a, bv, id_o, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar_o + 8 * pb);
-                    umma_commit(bar_empty + 8 * s);  // K_j and V_j are no longer read
+                umma_commit(bar_o + 8 * pb);
+                umma_commit(bar_vempty + 8 * va);
+                if (two) umma_commit(bar_vempty + 8 * vb);
+                va = vb + 1;
+                vph = vphb;
+                if (va == kVSlots) {
+                    va = 0;
+                    vph ^= 1;
                 }
-                __syncwarp();
             }
+            if (!ok) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
         }
-        if (!ok && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     } else {
         // ============================ softmax =============================
-        const int i = tid;  // query row of the tile, TMEM lane
+        // The two halves of a row agree on its maximum through shared memory
+        // (bounded mbarrier waits), so both use one reference.
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int i = quarter * 32 + lane;  // query row of the tile, TMEM lane
         const int pos = pos0 + i_first + i;
         const int vis = min(pos, kend - 1);
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        float* xmax = reinterpret_cast<float*>(smem + Smem::xch);  // [2][2][128]
+        float* xsum = xmax + 4 * kQTile;                            // [2][128]
+        {
+            // Q row i, dims 64 hf .. 64 hf + 63, into TMEM as fp16 pairs
+            uint32_t qv[32];
+            if (i < nq) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(qrow0 + i) * p.hq + h) * kHeadDim + hf * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = __ldg(src + c);
+                    qv[4 * c] = u.x; qv[4 * c + 1] = u.y; qv[4 * c + 2] = u.z; qv[4 * c + 3] = u.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) qv[c] = 0u;
+            }
+            tmem_st32(tmem + lane_base + kColQ + hf * 32, qv);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q);
+        }
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int kt = 0; kt < nkt && ok; ++kt) {
-            if (!(ok = mbar_wait(bar_s + 8 * (kt & 1), ((uint32_t)kt >> 1) & 1))) break;
+            if (!(ok = mbar_waitw(bar_s + 8 * (kt & 1), ((uint32_t)kt >> 1) & 1))) break;
             tc_fence_after();
             float s[64];
             {
-                uint32_t v[32];
+                uint32_t v0[32], v1[32];
+                tmem_ld64(tmem + lane_base + kColS + (kt & 1) * kKTile + hf * 64, v0, v1);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + (kt & 1) * kKTile + half * 32, v);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) s[half * 32 + c] = __uint_as_float(v[c]);
+                for (int c = 0; c < 32; ++c) {
+                    s[c] = __uint_as_float(v0[c]);
+                    s[32 + c] = __uint_as_float(v1[c]);
                 }
             }
-            const int t0 = kt * kKTile;
-            // Mask only where the tile reaches past this query's position
-            // (the diagonal tiles); scores stay unscaled until the exponent.
-            if (t0 + kKTile - 1 > vis) {
+            const int t0 = kt * kKTile + hf * 64;
+            if (t0 + 63 > vis) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) s[c] = t0 + c <= vis ? s[c] : -INFINITY;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            const float pm = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            xmax[((kt & 1) * 2 + hf) * kQTile + i] = pm;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_x + 8 * (kt & 1));
+            if (!(ok = mbar_waitw(bar_x + 8 * (kt & 1), ((uint32_t)kt >> 1) & 1))) break;
+            const float mx = fmaxf(pm, xmax[((kt & 1) * 2 + (hf ^ 1)) * kQTile + i]) * p.scale_log2;
             // Lazy rescaling: the reference maximum m only moves when a score
             // exceeds it by more than 2^8 (weights stay <= 256, exact enough in
             // fp16); the first tile sets it (key 0 is visible to every query).
@@ -393,43 +588,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
             // O is rescaled only after the previous PV product is complete.
             if (__any_sync(0xffffffffu, moved)) {
-                if (!(ok = mbar_wait(bar_o + 8 * ((kt - 1) & 1), ((uint32_t)(kt - 1) >> 1) & 1))) break;
+                if (!(ok = mbar_waitw(bar_o + 8 * ((kt - 1) & 1), ((uint32_t)(kt - 1) >> 1) & 1))) break;
                 tc_fence_after();
-                {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(t_o + lane_base + c0, v);
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kColO + hf * 64 + c0, v);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-                        tmem_st32(t_o + lane_base + c0, v);
-                    }
+                    for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+                    tmem_st32(tmem + lane_base + kColO + hf * 64 + c0, v);
                 }
             }
-            // P buffer kt & 1 was last read by the PV product of tile kt - 2.
-            if (kt >= 2) {
-                if (!(ok = mbar_wait(bar_o + 8 * (kt & 1), ((uint32_t)(kt - 2) >> 1) & 1))) break;
-            }
-            unsigned char* prow = smem + Smem::pbuf + (kt & 1) * (kQTile * 128) + i * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(prow + ((c ^ (i & 7)) << 4)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // P over the first 32 of this half's own 64 S columns (already read)
+            tmem_st32(tmem + lane_base + kColS + (kt & 1) * kKTile + hf * 64, pk);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p + 8 * (kt & 1));
         }
         // ---- finish: wait for the last PV product, normalise, store ----
-        if (ok) ok = mbar_wait(bar_o + 8 * ((nkt - 1) & 1), ((uint32_t)(nkt - 1) >> 1) & 1);
+        if (ok) ok = mbar_waitw(bar_o + 8 * ((nkt - 1) & 1), ((uint32_t)(nkt - 1) >> 1) & 1);
+        if (ok) {
+            xsum[hf * kQTile + i] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_l);
+            ok = mbar_waitw(bar_l, 0);
+        }
         if (ok) {
             tc_fence_after();
-            const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
-            __half* orow = p.out + ((int64_t)(qrow0 + i) * p.hq + h) * kHeadDim;
+            const float L = l + xsum[(hf ^ 1) * kQTile + i];
+            const float inv = L > 0.f ? __fdividef(1.f, L) : 0.f;
+            __half* orow = p.out + ((int64_t)(qrow0 + i) * p.hq + h) * kHeadDim + hf * 64;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld32(t_o + lane_base + c0, v);
+                tmem_ld32(tmem + lane_base + kColO + hf * 64 + c0, v);
                 if (i < nq) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
@@ -447,16 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- drain and release tensor memory ----
+    // ---- release tensor memory ----
     tc_fence_before();
     __syncthreads();
-    if (warp == kSoftWarps) {
-        // every armed stage's copies have landed before the block exits
-        for (int kt = max(0, nkt - kStages); kt < nkt; ++kt)
-            if (!mbar_wait(bar_full + 8 * (kt % kStages), ((uint32_t)kt / kStages) & 1) && lane == 0)
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-        if (!mbar_wait(bar_q, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-    }
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
@@ -474,28 +660,25 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
                       int max_seq_len, int32_t* dev_err, cudaStream_t stream) {
     using namespace prefill_tc;
     const int64_t pool_rows = (int64_t)num_blocks * block_size;
+    int kbox = kGranule;
+    while (kbox < kKTile && block_size % (2 * kbox) == 0) kbox *= 2;
+    const int vbox = kbox < 64 ? kbox : 64;
     const int64_t grid_x = ((int64_t)total_q + kQTile - 1) / kQTile + rows;
     if (pool_rows >= (int64_t(1) << 31) || grid_x >= (int64_t(1) << 31) || rows > kMaxRows)
         return PKV_ERR_UNSUPPORTED;
-    CUtensorMap qm, km, vm;
+    CUtensorMap km, vm;
     int st;
-    {
-        const int64_t dims[3] = {kHeadDim, q_heads, total_q};
-        const int64_t strides[2] = {kHeadDim * 2, (int64_t)q_heads * kHeadDim * 2};
-        const int box[3] = {64, 1, kQTile};
-        if ((st = tiled_map_3d(q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, box, &qm)) != PKV_OK)
-            return st;
-    }
     {
         const int64_t dims[3] = {kHeadDim, kv_heads, pool_rows};
         const int64_t strides[2] = {kHeadDim * 2, (int64_t)kv_heads * kHeadDim * 2};
-        const int box[3] = {64, 1, kGranule};
-        if ((st = tiled_map_3d(k_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, box, &km)) != PKV_OK)
+        const int kb[3] = {64, 1, kbox}, vb[3] = {64, 1, vbox};
+        if ((st = tiled_map_3d(k_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, kb, &km)) != PKV_OK)
             return st;
-        if ((st = tiled_map_3d(v_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, box, &vm)) != PKV_OK)
+        if ((st = tiled_map_3d(v_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, vb, &vm)) != PKV_OK)
             return st;
     }
     Params prm{};
+    prm.q = static_cast<const __half*>(q);
     prm.out = static_cast<__half*>(out);
     prm.tables = block_tables;
     prm.seq_lens = seq_lens;
@@ -507,17 +690,19 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
     prm.mbpr = max_blocks_per_row;
     prm.nb = num_blocks;
     prm.limit = max_seq_len;
+    prm.kbox = kbox;
+    prm.vbox = vbox;
     prm.scale_log2 = scale * kLog2e;
     prm.dev_err = dev_err;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Smem::total(kMaxRows)) != cudaSuccess)
+                                 Smem::total()) != cudaSuccess)
             return PKV_ERR_CUDA;
         attr_set = true;
     }
-    prefill_tc_kernel<<<dim3((unsigned)grid_x, (unsigned)q_heads), kThreads, Smem::total(rows), stream>>>(
-        qm, km, vm, prm);
+    prefill_tc_kernel<<<dim3((unsigned)grid_x, (unsigned)q_heads), kThreads, Smem::total(), stream>>>(
+        km, vm, prm);
     return launch_status();
 }
 

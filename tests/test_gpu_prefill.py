@@ -51,6 +51,8 @@ def run(case, q, qs, dev_err=None, tables=None):
     ([64, 300, 16], [17, 130, 16], 16),      # chunks at the end of longer rows
     ([1, 65, 200, 5], [1, 64, 65, 0], 64),   # a row with no queries
     ([640], [512], 32),                      # one 512-token chunk after 128 cached tokens
+    ([300, 129], [200, 129], 128),           # 128-token pages: one copy per K tile
+    ([260], [150], 48),                      # a page size that is no power of two
 ])
 def test_prefill_matches_oracle(cuda_device, lengths, chunks, bs):
     case, q, qs = prefill_case(lengths, chunks, bs, seed=sum(chunks) + bs)
