@@ -12,27 +12,28 @@
 // row's keys in 128-token tiles.  Warp roles:
 //   warps 0-7  softmax: warps w and w + 4 share query rows 32 (w % 4) .. (TMEM
 //              lanes); warp half hf = w / 4 takes tokens 64 hf .. 64 hf + 63 of
-//              each tile and head dims 64 hf .. 64 hf + 63 of Q and the output;
-//   warp 8     TMA: K tiles into a 4-slot ring;
+//              each tile and head dims 64 hf .. 64 hf + 63 of the output;
+//   warp 8     TMA: the queries once, then K tiles into a 3-slot ring;
 //   warp 9     TMA: V in 64-token halves into a 5-slot ring;
-//              each copy moves one box of 16, 32, 64 or 128 consecutive
+//              each K/V copy moves one box of 16, 32, 64 or 128 consecutive
 //              tokens of one page (the largest that divides the page size),
 //              its pool rows found through the block table;
-//   warp 10    S issue: S_t[128 q][128 tok] = Q . K_t^T, Q read from TMEM;
+//   warp 10    S issue: S_t[128 q][128 tok] = Q . K_t^T (both from shared memory);
 //   warp 11    PV issue: O[128 q][128 dims] += P_t . V_t, P read from TMEM.
 // One thread of each issuing warp drives tcgen05.mma (f16 in, f32
-// accumulate) and commits each group to an mbarrier.  The queries are
-// copied into TMEM once; S is double-buffered in TMEM and each softmax half
-// stores its fp16 probabilities over the first half of its own S columns, so
-// S_{t+2} reuses a buffer only after PV_t has read P_t.  Per tile a softmax
-// thread reads its half S row, applies the causal mask, agrees on the row
-// maximum with its partner warp, rescales its half O row in TMEM when the
-// maximum moved, and stores its P.  Shared memory holds only K and V, which
-// leaves its bandwidth to the copies and the B operands.  The producer and
-// issuer loops keep slots, parities and descriptors as running values: each
-// of those warps runs alone, so its loop is a chain of dependent
-// instructions.  Every wait sleeps in mbarrier.try_wait and is bounded in
-// wall time.
+// accumulate) and commits each group to an mbarrier.  S is triple-buffered
+// in TMEM and each softmax half stores its fp16 probabilities over the first
+// half of its own S columns, so S_{t+3} reuses a buffer only after PV_t has
+// read P_t: three tiles of slack between the softmax, the PV product and the
+// next S product.  Per tile a softmax thread reads its half S row, applies
+// the causal mask, agrees on the row maximum with its partner warp, rescales
+// its half O row in TMEM when the maximum moved, and stores its P.  The
+// producer and issuer loops keep slots, parities and descriptors as running
+// values: each of those warps runs alone, so its loop is a chain of
+// dependent instructions, and the tensor pipe only stays busy while the
+// issuing thread spends less than a product's time on each instruction
+// (full tiles take a branch-free issue path).  Every wait sleeps in
+// mbarrier.try_wait and is bounded in wall time.
 #include "pkv_internal.cuh"
 #include "ptx.cuh"
 
@@ -44,19 +45,20 @@ using namespace ptx;
 constexpr int kQTile = 128;
 constexpr int kKTile = 128;
 constexpr int kGranule = 16;  // the k-step of the PV product and the smallest copy box
-constexpr int kKSlots = 4;     // K ring, 128 tokens a slot; free once its S product is done
+constexpr int kKSlots = 3;     // K ring, 128 tokens a slot; free once its S product is done
 constexpr int kVSlots = 5;     // V ring, 64 tokens a slot; free once its PV product is done
+constexpr int kSBufs = 3;      // S buffers in TMEM
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = (kSoftWarps + 4) * 32;  // softmax, K TMA, V TMA, S issue, PV issue
 constexpr int kMaxRows = 1024;
+constexpr uint32_t kHalfQ = kQTile * 128;        // 128 queries x 64 dims
 constexpr uint32_t kKHalf = kKTile * 128;        // 128 tokens x 64 dims
 constexpr uint32_t kKSlot = 2 * kKHalf;          // K lo, K hi
 constexpr uint32_t kVHalf = 64 * 128;            // 64 tokens x 64 dims
 constexpr uint32_t kVSlot = 2 * kVHalf;          // V lo, V hi
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S buffers [0, 128), [128, 256); P over [0, 32) and [64, 96) of each
-constexpr uint32_t kColO = 256;  // O [256, 384)
-constexpr uint32_t kColQ = 384;  // Q [384, 448): fp16 pairs of head dims
+constexpr uint32_t kColS = 0;    // S buffers [0, 128), [128, 256), [256, 384); P over [0, 32) and [64, 96) of each
+constexpr uint32_t kColO = 384;  // O [384, 512)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
@@ -72,9 +74,10 @@ struct Params {
 };
 
 struct Smem {
-    static constexpr uint32_t kring = 0;                           // [K slots]
+    static constexpr uint32_t q = 0;                               // Q lo, Q hi
+    static constexpr uint32_t kring = q + 2 * kHalfQ;              // [K slots]
     static constexpr uint32_t vring = kring + kKSlots * kKSlot;    // [V slots]
-    static constexpr uint32_t bars = vring + kVSlots * kVSlot;     // 28 mbarriers
+    static constexpr uint32_t bars = vring + kVSlots * kVSlot;     // 29 mbarriers
     static constexpr uint32_t tmem = bars + 32 * 8;                // allocated TMEM address
     static constexpr uint32_t xch = tmem + 16;                     // row maxima [2][2][128], sums [2][128]
     // The tile scan's scratch (partials [threads], prefix [rows + 1]) lives
@@ -83,7 +86,7 @@ struct Smem {
     static constexpr uint32_t pre = part + kThreads * 4;
     __host__ __device__ static constexpr uint32_t total() { return xch + 6 * kQTile * 4 + 1024; }
 };
-static_assert(Smem::kring % 1024 == 0 && Smem::vring % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(Smem::kring % 1024 == 0 && Smem::vring % 1024 == 0 && (Smem::q + kHalfQ) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(Smem::pre + (kMaxRows + 1) * 4 <= Smem::kring + kKSlots * kKSlot, "scan scratch fits the K ring");
 static_assert(Smem::total() <= 232448, "shared memory per block");
 
@@ -202,20 +205,21 @@ __device__ __forceinline__ bool mbar_waitw(uint32_t bar, uint32_t parity) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const Params p) {
+                      const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap qmap, const Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_q = sbase + Smem::bars;               // Q copied into TMEM
+    const uint32_t bar_q = sbase + Smem::bars;               // queries landed
     const uint32_t bar_kfull = bar_q + 8;                    // [K slots]
     const uint32_t bar_kempty = bar_kfull + kKSlots * 8;     // [K slots]
     const uint32_t bar_vfull = bar_kempty + kKSlots * 8;     // [V slots]
     const uint32_t bar_vempty = bar_vfull + kVSlots * 8;     // [V slots]
-    const uint32_t bar_s = bar_vempty + kVSlots * 8;  // [2]: S buffer b computed (tiles b, b + 2, ...)
-    const uint32_t bar_p = bar_s + 16;  // [2]: P of S buffer b written
-    const uint32_t bar_o = bar_p + 16;  // [2]: PV product of P buffer b done
-    const uint32_t bar_x = bar_o + 16;  // [2]: both halves' row maxima of a tile written
+    const uint32_t bar_s = bar_vempty + kVSlots * 8;  // [3]: S buffer b computed (tiles b, b + 3, ...)
+    const uint32_t bar_p = bar_s + 8 * kSBufs;  // [3]: P of S buffer b written
+    const uint32_t bar_o = bar_p + 8 * kSBufs;  // [3]: PV product of buffer b done
+    const uint32_t bar_x = bar_o + 8 * kSBufs;  // [2]: both halves' row maxima of a tile written
     const uint32_t bar_l = bar_x + 16;  // both halves' row sums written
     uint32_t* sm_tmem = reinterpret_cast<uint32_t*>(smem + Smem::tmem);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- barriers and tensor memory (the scan scratch is dead from here) ----
     if (tid == 0) {
-        mbar_init(bar_q, kSoftWarps);
+        mbar_init(bar_q, 1);
         for (int s = 0; s < kKSlots; ++s) {
             mbar_init(bar_kfull + 8 * s, 1);
             mbar_init(bar_kempty + 8 * s, 1);
@@ -312,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_vempty + 8 * s, 1);
         }
         mbar_init(bar_l, kSoftWarps);
-        for (int b2 = 0; b2 < 2; ++b2) {
-            mbar_init(bar_x + 8 * b2, kSoftWarps);
-            mbar_init(bar_s + 8 * b2, 1);
-            mbar_init(bar_p + 8 * b2, kSoftWarps);
-            mbar_init(bar_o + 8 * b2, 1);
+        for (int b2 = 0; b2 < 2; ++b2) mbar_init(bar_x + 8 * b2, kSoftWarps);
+        for (int b3 = 0; b3 < kSBufs; ++b3) {
+            mbar_init(bar_s + 8 * b3, 1);
+            mbar_init(bar_p + 8 * b3, kSoftWarps);
+            mbar_init(bar_o + 8 * b3, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -345,6 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slot_bytes = is_v ? kVSlot : kKSlot;
         const uint32_t half_bytes = is_v ? kVHalf : kKHalf;
         const CUtensorMap* map = is_v ? &vmap : &kmap;
+        if (!is_v && lane == 0) {
+            mbar_arrive_expect_tx(bar_q, 2 * kHalfQ);
+            tma_load_3d(sbase + Smem::q, &qmap, 0, h, qrow0, bar_q);
+            tma_load_3d(sbase + Smem::q + kHalfQ, &qmap, 64, h, qrow0, bar_q);
+        }
         // Block-table entries are fetched a batch ahead: lane l handles box
         // l % gpu of unit l / gpu of a batch of 32 / gpu units, so the
         // table's latency is paid once per batch and hidden behind the
@@ -409,28 +418,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = max(0, nunits - nslots); u < nunits; ++u)
             if (!mbar_waitw(full0 + 8 * (u % nslots), (uint32_t)(u / nslots) & 1) && lane == 0)
                 flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+        if (!is_v && !mbar_waitw(bar_q, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     } else if (warp == kSoftWarps + 2) {
         // ============================ S issue ============================
-        // S_t = Q . K_t^T into S buffer t & 1, once K_t has landed and
-        // PV_{t-2} has read P_{t-2} out of that buffer.
+        // S_t = Q . K_t^T into S buffer t % 3, once K_t has landed and
+        // PV_{t-3} has read P_{t-3} out of that buffer.
         if (lane == 0) {
             const uint32_t id_s = idesc(kQTile, kKTile, 0);
             const uint64_t kd0 = sdesc(sbase + Smem::kring, 16, 1024);
             uint64_t kd = kd0;
+            const uint64_t qd = sdesc(sbase + Smem::q, 16, 1024);
             uint32_t kf = bar_kfull, ke = bar_kempty, ph = 0;
-            int s = 0;
+            int s = 0, sb = 0;
+            uint32_t sph = 0;  // use parity of S buffer sb
             bool ok = mbar_wait1(bar_q, 0);
             for (int t = 0; ok && t < nkt; ++t) {
                 if (!(ok = mbar_wait1(kf, ph))) break;
-                if (t >= 2 && !(ok = mbar_wait1(bar_o + 8 * (t & 1), (((uint32_t)t >> 1) & 1) ^ 1))) break;
+                if (t >= kSBufs && !(ok = mbar_wait1(bar_o + 8 * sb, sph ^ 1))) break;
                 tc_fence_after();
-                const uint32_t d = tmem + kColS + (t & 1) * kKTile;
+                const uint32_t d = tmem + kColS + sb * kKTile;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_ts(d, tmem + kColQ + ks * 8,
-                            kd + (uint64_t)((((ks >> 2) * kKHalf) + (ks & 3) * 32) >> 4), id_s, ks > 0);
-                umma_commit(bar_s + 8 * (t & 1));
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (uint32_t)((((ks >> 2) * kHalfQ) + (ks & 3) * 32) >> 4);
+                    umma_ss(d, qd + off, kd + off, id_s, ks > 0);
+                }
+                umma_commit(bar_s + 8 * sb);
                 umma_commit(ke);  // K_t is no longer read
+                if (++sb == kSBufs) {
+                    sb = 0;
+                    sph ^= 1;
+                }
                 if (++s == kKSlots) {
                     s = 0;
                     ph ^= 1;
@@ -456,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t vd0 = sdesc(sbase + Smem::vring, kVHalf, 1024);
             int va = 0;        // V slot of half 2 kt
             uint32_t vph = 0;  // its fill parity
+            int pb = 0;        // S buffer holding P_kt
+            uint32_t pph = 0;  // its use parity
             bool ok = true;
             for (int kt = 0; ok && kt < nkt; ++kt) {
                 int vb = va + 1;
@@ -479,19 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                const int pb = kt & 1;
-                if (!(ok = mbar_wait1(bar_p + 8 * pb, ((uint32_t)kt >> 1) & 1))) break;
+                if (!(ok = mbar_wait1(bar_p + 8 * pb, pph))) break;
                 tc_fence_after();
                 const uint32_t pa = tmem + kColS + pb * kKTile;
                 const uint64_t da = vd0 + (uint64_t)(va * (kVSlot >> 4));
                 const uint64_t db = vd0 + (uint64_t)(vb * (kVSlot >> 4));
+                // tokens 64 e .. 64 e + 63 sit in columns 64 e .. 64 e + 31
+                if (nsteps == 8 && kt > 0) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // tokens 64 e .. 64 e + 63 sit in columns 64 e .. 64 e + 31
-                    if (kk < nsteps)
+                    for (int kk = 0; kk < 8; ++kk)
                         umma_ts(tmem + kColO, pa + (kk >> 2) * 64 + (kk & 3) * 8,
-                                (kk < 4 ? da : db) + (uint64_t)((kk & 3) * 128), id_o,
-                                (kt > 0 || kk > 0) ? 1u : 0u);
+                                (kk < 4 ? da : db) + (uint64_t)((kk & 3) * 128), id_o, 1u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        if (kk < nsteps)
+                            umma_ts(tmem + kColO, pa + (kk >> 2) * 64 + (kk & 3) * 8,
+                                    (kk < 4 ? da : db) + (uint64_t)((kk & 3) * 128), id_o,
+                                    (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(bar_o + 8 * pb);
                 umma_commit(bar_vempty + 8 * va);
@@ -501,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (va == kVSlots) {
                     va = 0;
                     vph ^= 1;
+                }
+                if (++pb == kSBufs) {
+                    pb = 0;
+                    pph ^= 1;
                 }
             }
             if (!ok) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
@@ -516,35 +545,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         float* xmax = reinterpret_cast<float*>(smem + Smem::xch);  // [2][2][128]
         float* xsum = xmax + 4 * kQTile;                            // [2][128]
-        {
-            // Q row i, dims 64 hf .. 64 hf + 63, into TMEM as fp16 pairs
-            uint32_t qv[32];
-            if (i < nq) {
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(qrow0 + i) * p.hq + h) * kHeadDim + hf * 64);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 u = __ldg(src + c);
-                    qv[4 * c] = u.x; qv[4 * c + 1] = u.y; qv[4 * c + 2] = u.z; qv[4 * c + 3] = u.w;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) qv[c] = 0u;
-            }
-            tmem_st32(tmem + lane_base + kColQ + hf * 32, qv);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_q);
-        }
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        int sb = 0, psb = 0;          // S buffer of this tile and of the previous one
+        uint32_t sph = 0, psph = 0;   // their use parities
         for (int kt = 0; kt < nkt && ok; ++kt) {
-            if (!(ok = mbar_waitw(bar_s + 8 * (kt & 1), ((uint32_t)kt >> 1) & 1))) break;
+            if (!(ok = mbar_waitw(bar_s + 8 * sb, sph))) break;
             tc_fence_after();
             float s[64];
             {
                 uint32_t v0[32], v1[32];
-                tmem_ld64(tmem + lane_base + kColS + (kt & 1) * kKTile + hf * 64, v0, v1);
+                tmem_ld64(tmem + lane_base + kColS + sb * kKTile + hf * 64, v0, v1);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     s[c] = __uint_as_float(v0[c]);
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
             // O is rescaled only after the previous PV product is complete.
             if (__any_sync(0xffffffffu, moved)) {
-                if (!(ok = mbar_waitw(bar_o + 8 * ((kt - 1) & 1), ((uint32_t)(kt - 1) >> 1) & 1))) break;
+                if (!(ok = mbar_waitw(bar_o + 8 * psb, psph))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -600,14 +611,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // P over the first 32 of this half's own 64 S columns (already read)
-            tmem_st32(tmem + lane_base + kColS + (kt & 1) * kKTile + hf * 64, pk);
+            tmem_st32(tmem + lane_base + kColS + sb * kKTile + hf * 64, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p + 8 * (kt & 1));
+            if (lane == 0) mbar_arrive(bar_p + 8 * sb);
+            psb = sb;
+            psph = sph;
+            if (++sb == kSBufs) {
+                sb = 0;
+                sph ^= 1;
+            }
         }
         // ---- finish: wait for the last PV product, normalise, store ----
-        if (ok) ok = mbar_waitw(bar_o + 8 * ((nkt - 1) & 1), ((uint32_t)(nkt - 1) >> 1) & 1);
+        if (ok) ok = mbar_waitw(bar_o + 8 * psb, psph);
         if (ok) {
             xsum[hf * kQTile + i] = l;
             __syncwarp();
@@ -666,7 +683,7 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
     const int64_t grid_x = ((int64_t)total_q + kQTile - 1) / kQTile + rows;
     if (pool_rows >= (int64_t(1) << 31) || grid_x >= (int64_t(1) << 31) || rows > kMaxRows)
         return PKV_ERR_UNSUPPORTED;
-    CUtensorMap km, vm;
+    CUtensorMap km, vm, qm;
     int st;
     {
         const int64_t dims[3] = {kHeadDim, kv_heads, pool_rows};
@@ -675,6 +692,13 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
         if ((st = tiled_map_3d(k_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, kb, &km)) != PKV_OK)
             return st;
         if ((st = tiled_map_3d(v_pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, vb, &vm)) != PKV_OK)
+            return st;
+    }
+    {
+        const int64_t dims[3] = {kHeadDim, q_heads, total_q};
+        const int64_t strides[2] = {kHeadDim * 2, (int64_t)q_heads * kHeadDim * 2};
+        const int box[3] = {64, 1, kQTile};
+        if ((st = tiled_map_3d(q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dims, strides, box, &qm)) != PKV_OK)
             return st;
     }
     Params prm{};
@@ -702,7 +726,7 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
         attr_set = true;
     }
     prefill_tc_kernel<<<dim3((unsigned)grid_x, (unsigned)q_heads), kThreads, Smem::total(), stream>>>(
-        km, vm, prm);
+        km, vm, qm, prm);
     return launch_status();
 }
 
