@@ -351,7 +351,8 @@ def run_ours(args, rank, world, pg):
     ms_dec, _ = time_graph(g_dec, args.steps, args.warmup)
 
     # The same step over FP8 (E4M3) pools with one scale per KV head: per
-    # layer the quantising append and the FP8 decode (two launches, no PDL).
+    # layer one fused launch (quantising append + FP8 decode) with PDL, and
+    # for reference the two separate launches without PDL.
     gen8 = torch.Generator().manual_seed(args.seed + 8)
     kp8 = [torch.from_numpy(wl.fp8_codes(gen8, case.k_pool[l].shape)).to(dev) for l in range(L)]
     vp8 = [torch.from_numpy(wl.fp8_codes(gen8, case.v_pool[l].shape)).to(dev) for l in range(L)]
@@ -360,6 +361,12 @@ def run_ours(args, rank, world, pg):
 
     def step_fp8():
         for l in range(L):
+            ops.append_decode_fp8(out[l], d["q"][l], kp8[l], vp8[l], ks8, vs8, d["block_tables"],
+                                  d["seq_lens"], d["positions"], d["k_new"][l], d["v_new"][l],
+                                  case.scale, msl, ws, pdl=True)
+
+    def step_fp8_unfused():
+        for l in range(L):
             ops.append_fp8(kp8[l], vp8[l], ks8, vs8, d["block_tables"], d["positions"],
                            d["k_new"][l], d["v_new"][l])
             ops.decode_fp8(out[l], d["q"][l], kp8[l], vp8[l], ks8, vs8, d["block_tables"],
@@ -367,7 +374,10 @@ def run_ours(args, rank, world, pg):
 
     g8 = capture(step_fp8)
     ms8, _ = time_graph(g8, args.steps, args.warmup)
-    del g8, kp8, vp8
+    del g8
+    g8u = capture(step_fp8_unfused)
+    ms8u, _ = time_graph(g8u, args.steps, args.warmup)
+    del g8u, kp8, vp8
 
     # Chunked prefill: 8 rows whose newest 512 tokens (the pages' chunk size)
     # are the chunk, at 4096 tokens of context, one layer's pool.
@@ -429,8 +439,11 @@ def run_ours(args, rank, world, pg):
         "fp8_step": {"ms_per_step": round(ms8, 5),
                      "value": round(L * bytes8 / (ms8 * 1e-3) / 1e9, 2), "unit": "GB/s",
                      "bytes_per_layer": bytes8,
-                     "what": "per layer paged_kv_append_fp8 + paged_attention_decode_fp8 "
-                             "(E4M3 pools, one scale per KV head), no PDL"},
+                     "what": "per layer paged_attention_append_decode_fp8 with PDL "
+                             "(E4M3 pools, one scale per KV head)",
+                     "unfused_ms_per_step": round(ms8u, 5),
+                     "unfused_what": "per layer paged_kv_append_fp8 + paged_attention_decode_fp8, "
+                                     "no PDL"},
         "gpu_launches": args.steps * L,
         "clocks": clk,
     }

@@ -309,6 +309,34 @@ int paged_attention_decode_fp8(void* out, const void* q, const void* k_pool, con
                                void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                cudaStream_t stream);
 
+/*
+ * paged_attention_append_decode_fp8 -- one decode step of one layer over FP8
+ * pools: exactly paged_kv_append_fp8(k_pool, v_pool, k_scale, v_scale,
+ * block_tables, positions, k_new, v_new, ...) followed by
+ * paged_attention_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale,
+ * block_tables, seq_lens, ...), with the same arguments, results and errors
+ * as those two calls (the pools end bit-identical, the outputs equal those of
+ * the two calls).  Defining passages as for paged_attention_append_decode and
+ * the FP8 block above.  One launch: the new token is quantised and stored by
+ * the decode kernel, and the block that stages its slot takes the token's
+ * E4M3 values from k_new / v_new directly.  Supported shapes as for
+ * paged_attention_decode_fp8 (PKV_ERR_UNSUPPORTED otherwise); k_pool, v_pool,
+ * k_new and v_new need 16-byte alignment.
+ *
+ * flags: 0 or PKV_FLAG_PDL, as for paged_attention_append_decode; before the
+ * preceding kernel completes, a PDL launch also reads k_scale and v_scale,
+ * which that kernel must not write either.
+ */
+int paged_attention_append_decode_fp8(void* out, const void* q, void* k_pool, void* v_pool,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_tables, const int32_t* seq_lens,
+                                      const int32_t* positions, const void* k_new,
+                                      const void* v_new, int rows, int q_heads, int kv_heads,
+                                      int head_dim, int block_size, float scale,
+                                      int max_blocks_per_row, int num_blocks, int max_seq_len,
+                                      void* workspace, size_t workspace_bytes, unsigned flags,
+                                      int32_t* dev_err, cudaStream_t stream);
+
 /* Bytes of the static device scratch behind paged_attention_decode_noalloc
  * (8 MiB, held by every GPU that loads the library until the process exits). */
 #define PKV_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)

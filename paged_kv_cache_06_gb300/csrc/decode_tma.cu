@@ -47,6 +47,7 @@
 
 #include <mutex>
 
+#include "fp8_codec.cuh"
 #include "pkv_internal.cuh"
 #include "ptx.cuh"
 
@@ -324,12 +325,7 @@ __device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
         vc[k] = *reinterpret_cast<const uint4*>(slot + kBoxBytes + off);
     }
     __syncwarp();
-    auto widen = [](uint32_t w, uint32_t& lo, uint32_t& hi) {
-        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-            : "=r"(lo), "=r"(hi)
-            : "r"(w));
-    };
+    auto widen = [](uint32_t w, uint32_t& lo, uint32_t& hi) { widen4(w, lo, hi); };
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int i = lane + 32 * k, r = i >> 3, c = i & 7;
@@ -498,9 +494,11 @@ __device__ void make_plan(Plan& pl, const int* sm_pre, const int* sm_len, int ro
 // Per-row work of block cta, done by its producer warp after the dependency
 // wait (off the consumers' critical path): rows cta, cta + G, ... with nothing
 // to read get zero outputs, and in the fused form their new token is stored
-// into its slot.  The block that stages the slot's granule takes the token
-// from k_new / v_new directly, so the order of this store and that copy does
-// not matter.
+// into its slot (as E4M3 codes for FP8 pools, quantised exactly as
+// paged_kv_append_fp8 does).  The block that stages the slot's granule takes
+// the token from k_new / v_new directly, so the order of this store and that
+// copy does not matter.
+template <bool kFp8>
 __device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int lane) {
     for (int r = cta; r < p.rows; r += G) {
         if (sm_pre[r + 1] == sm_pre[r])
@@ -519,15 +517,18 @@ __device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int
             if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
             continue;
         }
-        const int vecs = p.hk * kHeadDim / 8;
+        const int vecs = p.hk * kHeadDim / 8;  // 8-element vectors per token and pool
         const int64_t dst = ((int64_t)pb * p.bs + pos % p.bs) * vecs;
         for (int i = lane; i < 2 * vecs; i += 32) {
-            if (i < vecs)
-                reinterpret_cast<uint4*>(p.kpool)[dst + i] =
-                    reinterpret_cast<const uint4*>(p.k_new)[(int64_t)r * vecs + i];
-            else
-                reinterpret_cast<uint4*>(p.vpool)[dst + i - vecs] =
-                    reinterpret_cast<const uint4*>(p.v_new)[(int64_t)r * vecs + i - vecs];
+            const bool is_v = i >= vecs;
+            const int j = is_v ? i - vecs : i;
+            const uint4 x = reinterpret_cast<const uint4*>(is_v ? p.v_new : p.k_new)[(int64_t)r * vecs + j];
+            if (kFp8) {
+                const float sc = (is_v ? p.v_scale : p.k_scale)[j / (kHeadDim / 8)];
+                reinterpret_cast<uint2*>(is_v ? p.vpool : p.kpool)[dst + j] = quantize8(x, sc);
+            } else {
+                reinterpret_cast<uint4*>(is_v ? p.vpool : p.kpool)[dst + j] = x;
+            }
         }
     }
 }
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ============================ producer ============================
         if (g0 >= g1) {
             griddep_wait();
-            if (kPaged) row_work(p, sm_pre, cta, G, lane);
+            if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
             return;
         }
         // Burst mode when the range fits the ring and covers at most
@@ -730,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             griddep_wait();
-            if (kPaged) row_work(p, sm_pre, cta, G, lane);
+            if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
             // Drain: every copy lands before the block exits.
             for (int j = 0; j < ng; ++j)
                 if (!mbar_wait(bar_slot + 8 * j, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
@@ -874,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
             }
         }
-        if (kPaged) row_work(p, sm_pre, cta, G, lane);
+        if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
         // Drain: the copies of every armed stage land before the block exits.
         for (int t = tile - kStages; t < tile; ++t) {
             if (t < 0) continue;
@@ -942,6 +943,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint4* src = reinterpret_cast<const uint4*>(
                     (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                 patch_val = src[lane & 15];
+                // FP8 pools hold the token as codes: take their exact fp16 values
+                if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
                 const int pos = p.positions[r];
                 if (pos >= 0 && us + pos / kGranule >= a && us + pos / kGranule < b) patch_tok = pos;
             }
@@ -1177,6 +1180,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const uint4* src = reinterpret_cast<const uint4*>(
                             (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                         patch_val = src[chunk];
+                        if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
                     }
                 }
             }
@@ -1456,7 +1460,7 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     using namespace tma;
     const bool paged = width == 0;
     const bool fp8 = k_scale != nullptr;
-    if (fp8 && (!paged || !v_scale || kv_heads > kFp8MaxKvHeads || append)) return PKV_ERR_UNSUPPORTED;
+    if (fp8 && (!paged || !v_scale || kv_heads > kFp8MaxKvHeads)) return PKV_ERR_UNSUPPORTED;
     const int64_t pool_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)rows * width;
     if (pool_rows >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
     const int limit = paged ? max_seq_len : width;

@@ -7,30 +7,9 @@
 // e4m3(c) * scale[head].  A new element x is stored as the nearest E4M3 value
 // (ties to even, saturating at 448) of the binary32 quotient x / scale.
 #include "pkv_internal.cuh"
+#include "fp8_codec.cuh"
 
 namespace pkv {
-
-// Two binary32 values to two E4M3 codes (round to nearest even, saturating);
-// lo lands in the lower byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t d;
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tmov.b16 %0, t;\n\t}"
-        : "=h"(d)
-        : "f"(hi), "f"(lo));
-    return d;
-}
-
-// Eight fp16 values (one 16-byte vector) to eight codes (8 bytes).
-__device__ __forceinline__ uint2 quantize8(uint4 x, float s) {
-    const __half2* h = reinterpret_cast<const __half2*>(&x);
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
-        w[i] = e4m3x2(__fdiv_rn(f.x, s), __fdiv_rn(f.y, s));
-    }
-    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-}
 
 // grid: rows; threads: (K or V, head, 8-dim chunk).
 __global__ void append_fp8_kernel(uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
@@ -119,4 +98,34 @@ extern "C" int paged_attention_decode_fp8(void* out, const void* q, const void* 
     return tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads, kv_heads,
                              block_size, scale, max_blocks_per_row, num_blocks, max_seq_len, 0,
                              workspace, dev_err, stream, nullptr, false, k_scale, v_scale);
+}
+
+extern "C" int paged_attention_append_decode_fp8(
+    void* out, const void* q, void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+    const int32_t* block_tables, const int32_t* seq_lens, const int32_t* positions, const void* k_new,
+    const void* v_new, int rows, int q_heads, int kv_heads, int head_dim, int block_size, float scale,
+    int max_blocks_per_row, int num_blocks, int max_seq_len, void* workspace, size_t workspace_bytes,
+    unsigned flags, int32_t* dev_err, cudaStream_t stream) {
+    using namespace pkv;
+    if (q_heads <= 0 || kv_heads <= 0 || head_dim <= 0 || q_heads % kv_heads) return PKV_ERR_INVALID_ARG;
+    if (rows < 0 || block_size <= 0 || block_size > 1024 || max_blocks_per_row <= 0 ||
+        num_blocks <= 0 || max_seq_len < 0 || !isfinite(scale) || (flags & ~PKV_FLAG_PDL))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_row * block_size) return PKV_ERR_INVALID_ARG;
+    if (!tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size) || kv_heads > 16)
+        return PKV_ERR_UNSUPPORTED;
+    if (rows == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !k_scale || !v_scale || !block_tables || !seq_lens ||
+        !positions || !k_new || !v_new)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len))
+        return PKV_ERR_WORKSPACE;
+    const AppendArgs app{positions, k_new, v_new};
+    return tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads, kv_heads,
+                             block_size, scale, max_blocks_per_row, num_blocks, max_seq_len, 0,
+                             workspace, dev_err, stream, &app, (flags & PKV_FLAG_PDL) != 0, k_scale,
+                             v_scale);
 }

@@ -77,6 +77,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, P,
                                              S, P, P]
     L.paged_attention_decode_fp8.restype = I
+    L.paged_attention_append_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
+                                                    F, I, I, I, P, S, ctypes.c_uint, P, P]
+    L.paged_attention_append_decode_fp8.restype = I
     L.paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P]
     L.paged_attention_prefill.restype = I
     L.paged_kv_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
@@ -291,6 +294,32 @@ def append_decode(out, q, k_pool, v_pool, block_tables, seq_lens, positions, k_n
         block_tables.shape[1], nb, int(max_seq_len), _ptr(workspace), workspace.numel(),
         PKV_FLAG_PDL if pdl else 0, _ptr(dev_err), _stream(stream))
     _check("paged_attention_append_decode", st)
+
+
+def append_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, positions,
+                      k_new, v_new, scale: float, max_seq_len: int, workspace, pdl: bool = False,
+                      dev_err=None, stream=None):
+    """paged_attention_append_decode_fp8: quantise and append each row's new
+    token into FP8 pools, then decode, in one launch (``pdl`` as for
+    append_decode)."""
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", torch.uint8, 4), (v_pool, "v_pool", torch.uint8, 4),
+                         (k_scale, "k_scale", torch.float32, 1), (v_scale, "v_scale", torch.float32, 1),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1),
+                         (positions, "positions", torch.int32, 1),
+                         (k_new, "k_new", torch.float16, 3), (v_new, "v_new", torch.float16, 3),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_append_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(seq_lens), _ptr(positions), _ptr(k_new), _ptr(v_new), rows, hq,
+        hk, d, bs, float(scale), block_tables.shape[1], nb, int(max_seq_len), _ptr(workspace),
+        workspace.numel(), PKV_FLAG_PDL if pdl else 0, _ptr(dev_err), _stream(stream))
+    _check("paged_attention_append_decode_fp8", st)
 
 
 def padded_decode(out, q, k_slab, v_slab, seq_lens, scale: float, workspace, dev_err=None,
