@@ -351,11 +351,12 @@ __device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
 }
 
 // Log-sum-exp merge of P partial records (children j = 0..P-1, rec_floats
-// apart) for head mh, dims md..md+7: M = max_j m_j, then
+// apart) for head mh, dims md..md+3 and md+64..md+67: M = max_j m_j, then
 // L = sum_j 2^(m_j - M) l_j and o = sum_j 2^(m_j - M) o_j, summed in child order
 // into two accumulator sets (even / odd j) added at the end.  The arithmetic
 // is the same whether the records are read from shared or global memory, so
-// the result never depends on which block merges.
+// the result never depends on which block merges.  The sixteen threads of a
+// head read 256 contiguous bytes per load.
 template <bool kGlobal>
 __device__ __forceinline__ void merge_children(const float* base, int P, int rec_floats, int mh,
                                                int md, float& Ls_out, float* acc) {
@@ -386,7 +387,7 @@ __device__ __forceinline__ void merge_children(const float* base, int P, int rec
                     w[c] = ld1(cr + mh);
                     l[c] = ld1(cr + 8 + mh);
                     x[c] = ld4(cr + kRecHead + mh * kHeadDim + md);
-                    y[c] = ld4(cr + kRecHead + mh * kHeadDim + md + 4);
+                    y[c] = ld4(cr + kRecHead + mh * kHeadDim + md + 64);
                 } else {
                     w[c] = -INFINITY;
                     l[c] = 0.f;
@@ -1363,7 +1364,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     const int mh = tid >> 4;        // head
-    const int md = (tid & 15) * 8;  // eight dims
+    const int md = (tid & 15) * 4;  // dims md..md+3 and md+64..md+67
     if (mh < p.group) {
         float Ls = 0.f, acc[8];
         if (landing)
@@ -1373,12 +1374,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             merge_children<true>(p.records + (int64_t)(cs + u) * p.rec_floats, P, p.rec_floats, mh,
                                  md, Ls, acc);
         const float iv = Ls > 0.f ? __fdividef(vs, Ls) : 0.f;
-        uint4 pk;
-        pk.x = pack_half2(acc[0] * iv, acc[1] * iv);
-        pk.y = pack_half2(acc[2] * iv, acc[3] * iv);
-        pk.z = pack_half2(acc[4] * iv, acc[5] * iv);
-        pk.w = pack_half2(acc[6] * iv, acc[7] * iv);
-        *reinterpret_cast<uint4*>(p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim + md) = pk;
+        __half* orow = p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim;
+        *reinterpret_cast<uint2*>(orow + md) =
+            make_uint2(pack_half2(acc[0] * iv, acc[1] * iv), pack_half2(acc[2] * iv, acc[3] * iv));
+        *reinterpret_cast<uint2*>(orow + md + 64) =
+            make_uint2(pack_half2(acc[4] * iv, acc[5] * iv), pack_half2(acc[6] * iv, acc[7] * iv));
     }
 }
 
