@@ -66,6 +66,7 @@ constexpr int kMaxRows = 1024;
 constexpr int kRecHead = 16;   // per record: m[8], l[8], then o[group][128]
 constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
 constexpr int kMergeBatch = 8; // children merged per register batch
+constexpr int kMergeBars = 4;  // landing barriers, one per batch (31 records fit the ring)
 constexpr int kBurstPieces = 4;
 constexpr int kBatch = 1;      // burst mode: granules per attend step (larger batches measured slower)
 constexpr int kCounterStride = 32;  // ints between the arrival counters of two units
@@ -122,7 +123,7 @@ struct Smem {
     static constexpr uint32_t comb = q + kStages * kQBytes;                         // [4][8][68] f32
     static constexpr uint32_t ml = comb + kConsumerWarps * 8 * kCombStride * 4;     // [4][8] m, [4][8] l
     static constexpr uint32_t bars = ml + 2 * kConsumerWarps * 8 * 4;               // full[S], empty[S], slot[R], merge
-    static constexpr uint32_t desc = bars + (2 * kStages + kRing + 2) * 8;          // TileDesc[S]
+    static constexpr uint32_t desc = bars + (2 * kStages + kRing + 1 + kMergeBars) * 8;  // TileDesc[S]
     static constexpr uint32_t plan = desc + kStages * 64;
     static constexpr uint32_t flags = plan + ((sizeof(Plan) + 15) / 16) * 16;       // misc ints
     static constexpr uint32_t scales = flags + 16 * 4;                              // FP8: k, v scale [2][16]
@@ -350,66 +351,65 @@ __device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
     __syncwarp();
 }
 
-// Log-sum-exp merge of P partial records (children j = 0..P-1, rec_floats
-// apart) for head mh, dims md..md+3 and md+64..md+67: M = max_j m_j, then
-// L = sum_j 2^(m_j - M) l_j and o = sum_j 2^(m_j - M) o_j, summed in child order
-// into two accumulator sets (even / odd j) added at the end.  The arithmetic
-// is the same whether the records are read from shared or global memory, so
-// the result never depends on which block merges.  The sixteen threads of a
-// head read 256 contiguous bytes per load.
+// One batch of the log-sum-exp merge of P partial records (children j0 ..
+// j0 + kMergeBatch - 1 of P, rec_floats apart) for head mh, dims md..md+3 and
+// md+64..md+67, merged online: M is the running maximum of the children's m;
+// when a batch raises it, what is summed so far is scaled by 2^(M_old - M),
+// then L += 2^(m_j - M) l_j and o += 2^(m_j - M) o_j in child order, into two
+// accumulator sets (even / odd j) added at the end.  The arithmetic is the
+// same whether the records are read from shared or global memory, so the
+// result never depends on which block merges.  The sixteen threads of a head
+// read 256 contiguous bytes per load.
 template <bool kGlobal>
-__device__ __forceinline__ void merge_children(const float* base, int P, int rec_floats, int mh,
-                                               int md, float& Ls_out, float* acc) {
+__device__ __forceinline__ void merge_batch(const float* base, int j0, int P, int rec_floats, int mh,
+                                            int md, float& M, float& Ls, float& Ls2, float* acc,
+                                            float* acc2) {
     auto ld1 = [&](const float* a) { return kGlobal ? __ldcg(a) : *a; };
     auto ld4 = [&](const float* a) {
         return kGlobal ? __ldcg(reinterpret_cast<const float4*>(a)) : *reinterpret_cast<const float4*>(a);
     };
-    float M = -INFINITY;
-    for (int j0 = 0; j0 < P; j0 += kMergeBatch) {
-        float t[kMergeBatch];
+    float w[kMergeBatch], l[kMergeBatch];
+    float4 x[kMergeBatch], y[kMergeBatch];
 #pragma unroll
-        for (int c = 0; c < kMergeBatch; ++c)
-            t[c] = j0 + c < P ? ld1(base + (int64_t)(j0 + c) * rec_floats + mh) : -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kMergeBatch; ++c) M = fmaxf(M, t[c]);
-    }
-    float acc2[8], Ls = 0.f, Ls2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = acc2[i] = 0.f;
-    if (M != -INFINITY) {
-        for (int j0 = 0; j0 < P; j0 += kMergeBatch) {
-            float w[kMergeBatch], l[kMergeBatch];
-            float4 x[kMergeBatch], y[kMergeBatch];
-#pragma unroll
-            for (int c = 0; c < kMergeBatch; ++c) {  // a batch's loads are in flight together
-                if (j0 + c < P) {
-                    const float* cr = base + (int64_t)(j0 + c) * rec_floats;
-                    w[c] = ld1(cr + mh);
-                    l[c] = ld1(cr + 8 + mh);
-                    x[c] = ld4(cr + kRecHead + mh * kHeadDim + md);
-                    y[c] = ld4(cr + kRecHead + mh * kHeadDim + md + 64);
-                } else {
-                    w[c] = -INFINITY;
-                    l[c] = 0.f;
-                    x[c] = y[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < kMergeBatch; c += 2) {
-                const float wa = fast_exp2(w[c] - M), wb = fast_exp2(w[c + 1] - M);
-                Ls += wa * l[c];
-                Ls2 += wb * l[c + 1];
-                acc[0] += wa * x[c].x; acc[1] += wa * x[c].y; acc[2] += wa * x[c].z; acc[3] += wa * x[c].w;
-                acc[4] += wa * y[c].x; acc[5] += wa * y[c].y; acc[6] += wa * y[c].z; acc[7] += wa * y[c].w;
-                acc2[0] += wb * x[c + 1].x; acc2[1] += wb * x[c + 1].y; acc2[2] += wb * x[c + 1].z;
-                acc2[3] += wb * x[c + 1].w; acc2[4] += wb * y[c + 1].x; acc2[5] += wb * y[c + 1].y;
-                acc2[6] += wb * y[c + 1].z; acc2[7] += wb * y[c + 1].w;
-            }
+    for (int c = 0; c < kMergeBatch; ++c) {  // a batch's loads are in flight together
+        if (j0 + c < P) {
+            const float* cr = base + (int64_t)(j0 + c) * rec_floats;
+            w[c] = ld1(cr + mh);
+            l[c] = ld1(cr + 8 + mh);
+            x[c] = ld4(cr + kRecHead + mh * kHeadDim + md);
+            y[c] = ld4(cr + kRecHead + mh * kHeadDim + md + 64);
+        } else {
+            w[c] = -INFINITY;
+            l[c] = 0.f;
+            x[c] = y[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    Ls_out = Ls + Ls2;
+    float Mb = M;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += acc2[i];
+    for (int c = 0; c < kMergeBatch; ++c) Mb = fmaxf(Mb, w[c]);
+    if (Mb == -INFINITY) return;
+    if (Mb > M) {
+        const float sc = M == -INFINITY ? 0.f : fast_exp2(M - Mb);
+        Ls *= sc;
+        Ls2 *= sc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[i] *= sc;
+            acc2[i] *= sc;
+        }
+        M = Mb;
+    }
+#pragma unroll
+    for (int c = 0; c < kMergeBatch; c += 2) {
+        const float wa = fast_exp2(w[c] - M), wb = fast_exp2(w[c + 1] - M);
+        Ls += wa * l[c];
+        Ls2 += wb * l[c + 1];
+        acc[0] += wa * x[c].x; acc[1] += wa * x[c].y; acc[2] += wa * x[c].z; acc[3] += wa * x[c].w;
+        acc[4] += wa * y[c].x; acc[5] += wa * y[c].y; acc[6] += wa * y[c].z; acc[7] += wa * y[c].w;
+        acc2[0] += wb * x[c + 1].x; acc2[1] += wb * x[c + 1].y; acc2[2] += wb * x[c + 1].z;
+        acc2[3] += wb * x[c + 1].w; acc2[4] += wb * y[c + 1].x; acc2[5] += wb * y[c + 1].y;
+        acc2[6] += wb * y[c + 1].z; acc2[7] += wb * y[c + 1].w;
+    }
 }
 
 // Burst plan for the block's range [g0, g1): its pieces (at most four) and
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         for (int s = 0; s < kRing; ++s) mbar_init(bar_slot + 8 * s, 1);
-        mbar_init(bar_merge, 1);
+        for (int b = 0; b < kMergeBars; ++b) mbar_init(bar_merge + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sm_flags[0] = 0;  // abort
         sm_flags[3] = 0;  // split pieces recorded ([4..13]: their unit, first block, pieces, row, head)
@@ -1348,32 +1348,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float vs = kFp8 ? sm_vs[kvh] : 1.f;
     const uint32_t rec_bytes = (uint32_t)p.rec_floats * 4u;
     // The ring is idle once the block's granules are consumed: the records
-    // land there by bulk copies issued at once.
+    // land there by bulk copies issued at once, in batches of kMergeBatch
+    // with a barrier each, and each batch is merged as soon as it has landed.
     const bool landing = (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
-    if (landing) {
-        if (warp == 0) {
-            if (lane == 0) mbar_arrive_expect_tx(bar_merge, (uint32_t)P * rec_bytes);
-            __syncwarp();
-            for (int j = lane; j < P; j += 32)
-                bulk_load(sbase + Smem::ring + j * rec_bytes,
-                          p.records + (int64_t)(cs + j + u) * p.rec_floats, rec_bytes, bar_merge);
-        }
-        if (!mbar_wait(bar_merge, 0)) {
-            if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            return;
-        }
+    if (landing && warp == 0) {
+        const int nbat = (P + kMergeBatch - 1) / kMergeBatch;
+        if (lane < nbat)
+            mbar_arrive_expect_tx(bar_merge + 8 * lane,
+                                  (uint32_t)min(kMergeBatch, P - lane * kMergeBatch) * rec_bytes);
+        __syncwarp();
+        for (int j = lane; j < P; j += 32)
+            bulk_load(sbase + Smem::ring + j * rec_bytes, p.records + (int64_t)(cs + j + u) * p.rec_floats,
+                      rec_bytes, bar_merge + 8 * (j / kMergeBatch));
     }
     const int mh = tid >> 4;        // head
     const int md = (tid & 15) * 4;  // dims md..md+3 and md+64..md+67
-    if (mh < p.group) {
-        float Ls = 0.f, acc[8];
-        if (landing)
-            merge_children<false>(reinterpret_cast<const float*>(smem + Smem::ring), P, p.rec_floats,
-                                  mh, md, Ls, acc);
-        else
-            merge_children<true>(p.records + (int64_t)(cs + u) * p.rec_floats, P, p.rec_floats, mh,
-                                 md, Ls, acc);
-        const float iv = Ls > 0.f ? __fdividef(vs, Ls) : 0.f;
+    const bool mine = mh < p.group;
+    float M = -INFINITY, Ls = 0.f, Ls2 = 0.f, acc[8], acc2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = acc2[i] = 0.f;
+    for (int j0 = 0; j0 < P; j0 += kMergeBatch) {
+        if (landing) {
+            if (!mbar_wait(bar_merge + 8 * (j0 / kMergeBatch), 0)) {
+                if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+                return;
+            }
+            if (mine)
+                merge_batch<false>(reinterpret_cast<const float*>(smem + Smem::ring), j0, P,
+                                   p.rec_floats, mh, md, M, Ls, Ls2, acc, acc2);
+        } else if (mine) {
+            merge_batch<true>(p.records + (int64_t)(cs + u) * p.rec_floats, j0, P, p.rec_floats, mh,
+                              md, M, Ls, Ls2, acc, acc2);
+        }
+    }
+    if (mine) {
+        const float L = Ls + Ls2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += acc2[i];
+        const float iv = L > 0.f ? __fdividef(vs, L) : 0.f;
         __half* orow = p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim;
         *reinterpret_cast<uint2*>(orow + md) =
             make_uint2(pack_half2(acc[0] * iv, acc[1] * iv), pack_half2(acc[2] * iv, acc[3] * iv));
