@@ -1352,14 +1352,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     // with a barrier each, and each batch is merged as soon as it has landed.
     const bool landing = (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
     if (landing && warp == 0) {
+        // a unit's records sit in consecutive workspace slots: one copy per batch
         const int nbat = (P + kMergeBatch - 1) / kMergeBatch;
-        if (lane < nbat)
-            mbar_arrive_expect_tx(bar_merge + 8 * lane,
-                                  (uint32_t)min(kMergeBatch, P - lane * kMergeBatch) * rec_bytes);
-        __syncwarp();
-        for (int j = lane; j < P; j += 32)
-            bulk_load(sbase + Smem::ring + j * rec_bytes, p.records + (int64_t)(cs + j + u) * p.rec_floats,
-                      rec_bytes, bar_merge + 8 * (j / kMergeBatch));
+        if (lane < nbat) {
+            const uint32_t bytes = (uint32_t)min(kMergeBatch, P - lane * kMergeBatch) * rec_bytes;
+            mbar_arrive_expect_tx(bar_merge + 8 * lane, bytes);
+            bulk_load(sbase + Smem::ring + lane * kMergeBatch * rec_bytes,
+                      p.records + (int64_t)(cs + u + lane * kMergeBatch) * p.rec_floats, bytes,
+                      bar_merge + 8 * lane);
+        }
     }
     const int mh = tid >> 4;        // head
     const int md = (tid & 15) * 4;  // dims md..md+3 and md+64..md+67
