@@ -416,8 +416,8 @@ __device__ __forceinline__ void merge_batch(const float* base, int j0, int P, in
 // the warps dealt to them.  Every piece gets one warp; each further warp goes
 // to the piece whose busiest warp has the most granules, while that is more
 // than one.  A piece's warps take near-equal contiguous shares of it.
-__device__ void make_plan(Plan& pl, const int* sm_pre, const int* sm_len, int rows, int hk, int g0,
-                          int g1, int W, int Geff) {
+__device__ void make_plan(Plan& pl, volatile int* flags, const int* sm_pre, const int* sm_len, int rows,
+                          int hk, int g0, int g1, int W, int Geff) {
     pl.burst = 0;
     pl.npieces = 0;
     for (int w = 0; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
@@ -490,6 +490,19 @@ __device__ void make_plan(Plan& pl, const int* sm_pre, const int* sm_len, int ro
     for (; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
     pl.npieces = k;
     pl.burst = 1;
+    // the split pieces, recorded now for the tail (their unit, first block,
+    // pieces, row, head)
+    int ks = 0;
+    for (int i = 0; i < k; ++i) {
+        if (pl.P[i] == 1) continue;
+        flags[4 + 5 * ks] = pl.r[i] * hk + pl.kvh[i];
+        flags[5 + 5 * ks] = pl.cstart[i];
+        flags[6 + 5 * ks] = pl.P[i];
+        flags[7 + 5 * ks] = pl.r[i];
+        flags[8 + 5 * ks] = pl.kvh[i];
+        ++ks;
+    }
+    flags[3] = ks;
 }
 
 // Per-row work of block cta, done by its producer warp after the dependency
@@ -887,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ============================== consumers ==============================
-    if (tid == 0) make_plan(*sm_plan, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
+    if (tid == 0) make_plan(*sm_plan, sm_flags, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
     consumer_sync();
     const bool burst = sm_plan->burst != 0;
     if (burst && sm_plan->wpiece[warp] >= 0) {
@@ -1038,10 +1051,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                     yw[w] = *reinterpret_cast<const float4*>(dw + kRecHead + h * kDumpStride + 8 * c + 4);
                 }
             }
+            int pw0[kBurstPieces], pwn[kBurstPieces], pr[kBurstPieces], pkv[kBurstPieces], pP[kBurstPieces];
 #pragma unroll
             for (int pc = 0; pc < kBurstPieces; ++pc) {
-                if (pc >= pl.npieces || h >= gsz) break;
-                const int w0 = pl.w0[pc], w1 = w0 + pl.wn[pc];
+                pw0[pc] = pl.w0[pc];
+                pwn[pc] = pl.wn[pc];
+                pr[pc] = pl.r[pc];
+                pkv[pc] = pl.kvh[pc];
+                pP[pc] = pl.P[pc];
+            }
+            const int npc = h < gsz ? pl.npieces : 0;
+#pragma unroll
+            for (int pc = 0; pc < kBurstPieces; ++pc) {
+                if (pc >= npc) break;
+                const int w0 = pw0[pc], w1 = w0 + pwn[pc];
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w)
@@ -1057,8 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     acc[0] += wt * xw[w].x; acc[1] += wt * xw[w].y; acc[2] += wt * xw[w].z; acc[3] += wt * xw[w].w;
                     acc[4] += wt * yw[w].x; acc[5] += wt * yw[w].y; acc[6] += wt * yw[w].z; acc[7] += wt * yw[w].w;
                 }
-                const int r = pl.r[pc], kvh = pl.kvh[pc];
-                if (pl.P[pc] == 1) {
+                const int r = pr[pc], kvh = pkv[pc];
+                if (pP[pc] == 1) {
                     const float inv = L > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, L) : 0.f;
                     uint4 pk;
                     pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
@@ -1078,19 +1101,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                         make_float4(acc[4], acc[5], acc[6], acc[7]);
                 }
             }
-        }
-        if (tid == 0) {
-            int k = 0;
-            for (int pc = 0; pc < pl.npieces; ++pc) {
-                if (pl.P[pc] == 1) continue;
-                sm_flags[4 + 5 * k] = pl.r[pc] * hk + pl.kvh[pc];
-                sm_flags[5 + 5 * k] = pl.cstart[pc];
-                sm_flags[6 + 5 * k] = pl.P[pc];
-                sm_flags[7 + 5 * k] = pl.r[pc];
-                sm_flags[8 + 5 * k] = pl.kvh[pc];
-                ++k;
-            }
-            sm_flags[3] = k;
         }
     } else {
         // ============================ stream mode ============================
