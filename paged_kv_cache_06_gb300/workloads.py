@@ -297,7 +297,7 @@ def custom(lengths, block_size: int, seed: int = 0, layers: int = 1, append: boo
                       kv_heads=kv_heads, head_dim=head_dim)
 
 
-CONFIGS = {
+WORKLOADS = {
     "tiny": tiny,
     "uniform": uniform,
     "mixed": mixed,

@@ -184,9 +184,9 @@ def test_padded_comparator_matches_oracle(cuda_device):
 @pytest.mark.parametrize("name", ["uniform", "mixed", "shared", "long"])
 def test_full_size_workloads_sampled(cuda_device, name):
     if name in ("uniform", "mixed"):
-        case = wl.CONFIGS[name](layers=1)
+        case = wl.WORKLOADS[name](layers=1)
     else:
-        case = wl.CONFIGS[name]()
+        case = wl.WORKLOADS[name]()
     out, *_ = run_gpu(case)
     L = case.seq_lens
     rows = sorted({int(np.argmax(L)), int(np.argmin(L)), 0, case.rows - 1, case.rows // 2})
