@@ -191,7 +191,7 @@ def decode_source_hash() -> str:
     csrc = os.path.join(ROOT, "paged_kv_cache_06_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if (name.startswith("decode") and name.endswith((".cu", ".cuh"))) or \
-                name in ("ptx.cuh", "pkv_internal.cuh", "tmap.cu"):
+                name in ("ptx.cuh", "pkv_internal.cuh", "tmap.cu", "fp8_codec.cuh"):
             h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 

@@ -66,7 +66,8 @@ constexpr int kMaxRows = 1024;
 constexpr int kRecHead = 16;   // per record: m[8], l[8], then o[group][128]
 constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
 constexpr int kMergeBatch = 8; // children merged per register batch
-constexpr int kMergeBars = 4;  // landing barriers, one per batch (31 records fit the ring)
+constexpr int kMergeBars = 4;  // landing barriers, one per batch
+constexpr int kLandMax = kMergeBars * kMergeBatch;  // most records a landed merge takes
 constexpr int kBurstPieces = 4;
 constexpr int kBatch = 1;      // burst mode: granules per attend step (larger batches measured slower)
 constexpr int kCounterStride = 32;  // ints between the arrival counters of two units
@@ -1360,7 +1361,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     // The ring is idle once the block's granules are consumed: the records
     // land there by bulk copies issued at once, in batches of kMergeBatch
     // with a barrier each, and each batch is merged as soon as it has landed.
-    const bool landing = (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
+    // A unit with more records than the ring or the barriers take is merged
+    // from the workspace directly.
+    const bool landing =
+        P <= kLandMax && (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
     if (landing && warp == 0) {
         // a unit's records sit in consecutive workspace slots: one copy per batch
         const int nbat = (P + kMergeBatch - 1) / kMergeBatch;

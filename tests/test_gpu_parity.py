@@ -161,6 +161,30 @@ def test_workspace_reuse_gives_identical_results(cuda_device):
         assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+@pytest.mark.parametrize("lengths,hq,hk", [
+    ([8192], 4, 2),                    # group of 2: each unit split over 76 blocks
+    ([3000, 2000], 2, 2),              # group of 1: 46-47 pieces, then 31
+    ([1000, 1000, 1000, 1000], 2, 2),  # group of 1: 19 pieces per unit, landed merges
+    ([1100, 1100], 8, 2),              # group of 4: 38 pieces per unit
+    ([4096, 40, 900], 8, 2),           # group of 4: ~62 pieces on the long row, ~15 on the last
+])
+def test_units_split_over_many_blocks_small_groups(cuda_device, lengths, hq, hk):
+    """A unit's merge over many pieces, for every record size: landed in shared
+    memory when its records fit, else read from the workspace; repeated calls
+    on one workspace stay bit-identical (arrival words re-armed)."""
+    case = wl.custom(lengths, 16, seed=len(lengths) + hq, nan_fill=True, q_heads=hq, kv_heads=hk)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, kp, vp, d, ws = run_gpu(case, dev_err=err)
+    _, _, ref = oracle_after_append(case, 0)
+    assert_close(out, ref, f"lengths={lengths} hq={hq} hk={hk}")
+    for _ in range(3):
+        out2 = torch.full_like(out, float("nan"))
+        ops.decode(out2, d["q"][0], kp, vp, d["block_tables"], d["seq_lens"], case.scale,
+                   case.max_seq_len, ws, dev_err=err)
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert int(err.item()) == 0
+
+
 def test_padded_comparator_matches_oracle(cuda_device):
     case = wl.custom([12, 300, 1, 257], 16, seed=7, nan_fill=True)
     _, _, ref = oracle_after_append(case, 0)
