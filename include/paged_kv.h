@@ -262,7 +262,17 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
  * (host value, sizes the launch).  A row with C_r > seq_lens[r] or
  * seq_lens[r] > max_seq_len is skipped (its outputs untouched) and flagged
  * PKV_DEV_ERR_SEQ_LEN; table entries as in paged_attention_decode.  Supported
- * for head_dim 128, block_size a multiple of 16, rows <= 1024.  No workspace.
+ * for head_dim 128, block_size a multiple of 16, rows <= 1024, and at most
+ * 2^31 key-tile steps in total (q_heads x 128-query tiles x 128-key tiles;
+ * PKV_ERR_UNSUPPORTED beyond).
+ *
+ * No caller workspace: one block per SM splits the steps evenly, and a
+ * 128-query tile cut between two blocks is merged through a partial result
+ * kept in library-owned device memory (about 13 MB per device, allocated when
+ * the library loads).  So prefill calls on one device must not overlap each
+ * other: issue them on one stream, or order the streams.  Each call leaves that
+ * memory ready for the next; after a PKV_DEV_ERR_TIMEOUT its arrival counters
+ * may not be, and later prefill results on that device are not reliable.
  */
 int paged_attention_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* block_tables, const int32_t* seq_lens,

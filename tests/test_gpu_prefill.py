@@ -53,6 +53,11 @@ def run(case, q, qs, dev_err=None, tables=None):
     ([640], [512], 32),                      # one 512-token chunk after 128 cached tokens
     ([300, 129], [200, 129], 128),           # 128-token pages: one copy per K tile
     ([260], [150], 48),                      # a page size that is no power of two
+    ([192], [128], 16),                      # every unit cut in two; the end piece starts past
+                                             #   the first 64 queries' last key
+    ([8192], [128], 64),                     # one query tile per head, its keys cut over ~13 blocks
+    ([3000, 20, 2500], [700, 20, 300], 16),  # long and short units cut at arbitrary steps
+    ([20] * 60, [5] * 60, 16),               # many short units per block
 ])
 def test_prefill_matches_oracle(cuda_device, lengths, chunks, bs):
     case, q, qs = prefill_case(lengths, chunks, bs, seed=sum(chunks) + bs)
@@ -99,3 +104,15 @@ def test_prefill_bad_chunk_is_flagged_and_skipped(cuda_device):
                                case.seq_lens[1:], qs[1:] - 12, case.scale)
     assert_close(out[12:], ref, "the valid row")
     assert torch.isnan(out[:12].float()).all()  # skipped row untouched
+
+
+def test_prefill_repeated_calls_are_bit_identical(cuda_device):
+    """Units cut over several blocks merge the same way on every call (the
+    arrival words are left at zero for the next call)."""
+    case, q, qs = prefill_case([4000, 900], [256, 300], 32, seed=15)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = run(case, q, qs, dev_err=err)
+    for _ in range(3):
+        again = run(case, q, qs, dev_err=err)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    assert int(err.item()) == 0
