@@ -95,6 +95,7 @@ struct Params {
     int rows, hq, group, bs, mbpr, nb, limit;
     int kbox, vbox;  // tokens per K and V copy
     float scale_log2;
+    int out_v8;      // out is 32-byte aligned: 32-byte stores
     float* part;     // [grid][kPartFloats]: the partial of each block's cut unit
     int* count;      // [grid][kCountStride]: pieces arrived for the unit a block merges (zero between calls)
     int32_t* dev_err;
@@ -279,6 +280,13 @@ __device__ __forceinline__ bool mbar_drain1(uint32_t bar, uint32_t parity) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
     } while (now_ns() - t0 < kWaitLimitNs);
     return false;
+}
+
+// Sixteen fp16 outputs (8 words) to a 32-byte-aligned address.
+__device__ __forceinline__ void st_v8(void* dst, const uint32_t (&u)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(u[0]), "r"(u[1]),
+                 "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7])
+                 : "memory");
 }
 
 // Bring a query tile (both 64-dim halves) into L2 ahead of its load.
@@ -890,7 +898,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_odrained);
-                if (i < nq) {
+                if (i < nq && p.out_v8) {
+#pragma unroll
+                    for (int c = 0; c < 64; c += 16) {
+                        const uint32_t* u = c < 32 ? v + c : v2 + (c - 32);
+                        uint32_t w8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w8[e] = pack_half2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+                        st_v8(orow + c, w8);
+                    }
+                } else if (i < nq) {
 #pragma unroll
                     for (int c = 0; c < 64; c += 8) {
                         const uint32_t* u = c < 32 ? v + c : v2 + (c - 32);
@@ -987,7 +1005,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[c + 3] += wj * x.w;
                         }
                     }
-                    if (i < nq) {
+                    if (i < nq && p.out_v8) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 16) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w8[e] = pack_half2(acc[c + 2 * e] * inv, acc[c + 2 * e + 1] * inv);
+                            st_v8(orow + c0 + c, w8);
+                        }
+                    } else if (i < nq) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             uint4 q4;
@@ -1123,6 +1149,7 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
     prm.kbox = kbox;
     prm.vbox = vbox;
     prm.scale_log2 = scale * kLog2e;
+    prm.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
     prm.part = dv.part;
     prm.count = dv.count;
     prm.dev_err = dev_err;

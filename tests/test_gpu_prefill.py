@@ -116,3 +116,22 @@ def test_prefill_repeated_calls_are_bit_identical(cuda_device):
         again = run(case, q, qs, dev_err=err)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert int(err.item()) == 0
+
+
+def test_prefill_output_aligned_to_16_bytes_only(cuda_device):
+    """An output that is 16- but not 32-byte aligned takes 16-byte stores."""
+    case, q, qs = prefill_case([700, 300], [300, 129], 32, seed=16)
+    d = wl.to_device(case)
+    gq = torch.from_numpy(q.view(np.int16)).view(torch.float16).cuda()
+    big = torch.full((gq.numel() + 8,), float("nan"), dtype=torch.float16, device="cuda")
+    out = big[8:].view(gq.shape)
+    assert out.data_ptr() % 32 == 16
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.prefill(out, gq, d["k_pool"][0], d["v_pool"][0], d["block_tables"], d["seq_lens"],
+                torch.from_numpy(qs).cuda(), case.scale, case.max_seq_len, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isnan(big[:8].float()).all()
+    ref = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables, case.seq_lens,
+                               qs, case.scale, num_threads=oracle.default_threads())
+    assert_close(out, ref, "16-byte aligned output")
