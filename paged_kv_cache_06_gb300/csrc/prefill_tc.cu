@@ -21,9 +21,11 @@
 // segments from the last to the first: the piece that ends a split unit is
 // the first segment of its block's range, so it is processed last, while the
 // unit's other pieces are the last segments of the blocks before, processed
-// first.  The end piece's block merges: it waits (bounded) until the other
-// pieces have counted themselves on its arrival word, then combines their
-// partials with its own state before it normalises and stores.
+// first.  The end piece's block merges: once its S products are done, its
+// S-issue thread waits (bounded) until the other pieces have counted
+// themselves on its arrival word and lands the first other piece's partial in
+// the idle K ring with one bulk copy; the softmax warps then combine the
+// partials with their own state before they normalise and store.
 //
 // Warp roles (each walks the same segments):
 //   warps 0-7  softmax: warps w and w + 4 share query rows 32 (w % 4) .. (TMEM
@@ -289,7 +291,7 @@ __device__ __forceinline__ void st_v8(void* dst, const uint32_t (&u)[8]) {
                  : "memory");
 }
 
-// Bring a query tile (both 64-dim halves) into L2 ahead of its load.
+// Bring one box of a tensor map into L2 ahead of its load.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
