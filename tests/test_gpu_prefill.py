@@ -135,3 +135,25 @@ def test_prefill_output_aligned_to_16_bytes_only(cuda_device):
     ref = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables, case.seq_lens,
                                qs, case.scale, num_threads=oracle.default_threads())
     assert_close(out, ref, "16-byte aligned output")
+
+
+def test_prefill_1024_rows_of_short_chunks(cuda_device):
+    """The most rows the kernel takes, with tiny ragged chunks (some empty):
+    many whole units per block and rows skipped by the walk."""
+    rng = np.random.default_rng(17)
+    lengths = rng.integers(1, 40, size=1024)
+    chunks = np.minimum(lengths, rng.integers(0, 4, size=1024))
+    case, q, qs = prefill_case(lengths.tolist(), chunks.tolist(), 16, seed=17)
+    ref = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables, case.seq_lens,
+                               qs, case.scale, num_threads=oracle.default_threads())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(case, q, qs, dev_err=err)
+    assert int(err.item()) == 0
+    assert_close(out, ref, "1024 rows")
+
+
+def test_prefill_more_than_1024_rows_is_rejected(cuda_device):
+    case, q, qs = prefill_case([3] * 1025, [1] * 1025, 16, seed=18)
+    with pytest.raises(ops.PagedKVError) as e:
+        run(case, q, qs)
+    assert e.value.status == 2  # PKV_ERR_UNSUPPORTED
