@@ -215,7 +215,12 @@ def decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
 
 def prefill(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: float,
             max_seq_len: int, dev_err=None, stream=None):
-    """paged_attention_prefill: causal attention of each row's chunk of new tokens."""
+    """paged_attention_prefill: causal attention of each row's chunk of new tokens.
+
+    The kernel keeps the partial results of query tiles cut between blocks
+    in library-owned device memory, so prefill calls on one device must not
+    overlap: issue them on one stream, or order the streams.
+    """
     for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
                          (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
                          (block_tables, "block_tables", torch.int32, 2),
