@@ -288,15 +288,34 @@ def run_ours(args, rank, world, pg):
     rows, hq, hk, hd = case.rows, case.q_heads, case.kv_heads, case.head_dim
     msl = case.max_seq_len
     ws = ops.alloc_workspace(rows, hq, hk, hd, msl, case.block_size, device=dev)
+    plan_buf = ops.alloc_plan(rows, hq, hk, hd, msl, case.block_size, device=dev)
     out = torch.zeros(L, rows, hq, hd, dtype=torch.float16, device=dev)
 
+    def make_plan():
+        ops.plan(plan_buf, d["block_tables"], d["seq_lens"], d["positions"], hq, hk, hd,
+                 case.block_size, case.num_blocks, msl)
+
     def step():
-        # One layer = one fused launch (append the new token, decode); layers
-        # overlap their prologues through programmatic dependent launch.
+        # One layer = one fused launch (append the new token, decode); each
+        # block derives the step's split itself before its dependency wait,
+        # and layers overlap through programmatic dependent launch.
         for l in range(L):
             ops.append_decode(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l],
                               d["block_tables"], d["seq_lens"], d["positions"], d["k_new"][l],
                               d["v_new"][l], case.scale, msl, ws, pdl=True)
+
+    def step_planned():
+        # The step's work split is planned once; then one fused launch per
+        # layer, each overlapping the previous one through programmatic
+        # dependent launch (the first follows the plan without it, since it
+        # reads the plan early).
+        make_plan()
+        for l in range(L):
+            ops.decode_planned(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l],
+                               d["block_tables"], d["seq_lens"], case.scale, msl, plan_buf, ws,
+                               positions=d["positions"], k_new=d["k_new"][l], v_new=d["v_new"][l],
+                               pdl=l > 0)
+
 
     def step_unfused():
         for l in range(L):
@@ -306,9 +325,10 @@ def run_ours(args, rank, world, pg):
                        d["seq_lens"], case.scale, msl, ws)
 
     def decode_only():
+        make_plan()
         for l in range(L):
-            ops.decode(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l], d["block_tables"],
-                       d["seq_lens"], case.scale, msl, ws)
+            ops.decode_planned(out[l], d["q"][l], d["k_pool"][l], d["v_pool"][l],
+                               d["block_tables"], d["seq_lens"], case.scale, msl, plan_buf, ws)
 
     def capture(fn):
         fn()  # eager warm-up (also validates arguments)
@@ -360,6 +380,9 @@ def run_ours(args, rank, world, pg):
     g_unf = capture(step_unfused)
     ms_unf, _ = time_graph(g_unf, args.steps, args.warmup)
     del g_unf
+    g_pl = capture(step_planned)
+    ms_pl, _ = time_graph(g_pl, args.steps, args.warmup)
+    del g_pl
     g_dec = capture(decode_only)
     ms_dec, _ = time_graph(g_dec, args.steps, args.warmup)
 
@@ -434,6 +457,11 @@ def run_ours(args, rank, world, pg):
                      "kernel": "paged_attention_append_decode (fused, PDL)",
                      "bytes_per_launch": bytes_launch,
                      "launch_us": round(per_launch_s * 1e6, 3)},
+        "planned_step": {"ms_per_step": round(ms_pl, 5),
+                         "value": round(total_bytes / (ms_pl * 1e-3) / 1e9 if world == 1 else 0, 2),
+                         "what": "paged_attention_plan once, then per layer "
+                                 "paged_attention_decode_planned (fused append + decode, PDL "
+                                 "from layer 1)"},
         "unfused_step": {"ms_per_step": round(ms_unf, 5),
                          "value": round(total_bytes / (ms_unf * 1e-3) / 1e9 if world == 1 else 0, 2),
                          "what": "per layer paged_kv_append + paged_attention_decode, no PDL"},

@@ -71,6 +71,7 @@ typedef enum {
 #define PKV_DEV_ERR_SEQ_LEN 0x2  /* seq_len < 0, > max_seq_len or > max_blocks_per_row * block_size */
 #define PKV_DEV_ERR_POSITION 0x4 /* append position's logical block >= max_blocks_per_row */
 #define PKV_DEV_ERR_TIMEOUT 0x8  /* a bounded wait inside a kernel gave up (the call's output is invalid) */
+#define PKV_DEV_ERR_PLAN 0x10    /* a decode plan made for another launch size was passed (nothing was done) */
 
 /* Human-readable name of a pkv_status.  Never null; static storage. */
 const char* pkv_status_string(int status);
@@ -346,6 +347,70 @@ int paged_attention_append_decode_fp8(void* out, const void* q, void* k_pool, vo
                                       int max_blocks_per_row, int num_blocks, int max_seq_len,
                                       void* workspace, size_t workspace_bytes, unsigned flags,
                                       int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * Decode plans.  The work of a decode step is split over one thread block per
+ * SM by cutting every row's tokens, in 16-token granules, into equal
+ * contiguous ranges; each block then gathers the K/V blocks of its range
+ * through the rows' block tables ("PagedAttention", deepconcepts.dev, section
+ * "PagedAttention": walk the table, gather only the listed blocks), and rows
+ * cut between blocks are merged exactly through their log-sum-exp (its
+ * closing note on FlashAttention).  Every layer of a step reads the same rows
+ * at the same lengths through the same tables, so that split -- each block's
+ * range, the rows and heads it serves, the physical rows of its granules, and
+ * which block holds each row's appended token -- is the same for all of them.
+ * paged_attention_plan makes it once per step; paged_attention_decode_planned
+ * then starts each layer's copies straight from it instead of re-deriving it
+ * from seq_lens and the tables.
+ *
+ * paged_attention_plan_size -- bytes of a plan for these sizes (an upper
+ * bound independent of the device), or 0 when the staged decode kernel does
+ * not take the shape (then plan nothing and call the unplanned entry points).
+ */
+size_t paged_attention_plan_size(int rows, int q_heads, int kv_heads, int head_dim,
+                                 int max_seq_len, int block_size);
+
+/*
+ * paged_attention_plan -- write the plan of one decode step into `plan`
+ * (device buffer of paged_attention_plan_size(...) bytes, caller-owned).  One
+ * small launch on `stream`.  block_tables, seq_lens, positions and the sizes
+ * are those every planned call of the step will pass; positions may be null
+ * when the step appends nothing.  A seq_len outside [0, max_seq_len] and table
+ * entries outside [0, num_blocks) are flagged here (PKV_DEV_ERR_SEQ_LEN /
+ * PKV_DEV_ERR_BLOCK_ID), and the granules concerned are planned as empty.
+ * The plan stays valid while those inputs do not change.
+ */
+int paged_attention_plan(void* plan, size_t plan_bytes, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int32_t* positions, int rows, int q_heads,
+                         int kv_heads, int head_dim, int block_size, int max_blocks_per_row,
+                         int num_blocks, int max_seq_len, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * paged_attention_decode_planned -- one layer of a planned step: the same
+ * result as paged_attention_append_decode (positions non-null) or
+ * paged_attention_decode (positions null; k_new, v_new unused), over fp16
+ * pools (k_scale == v_scale == null) or FP8 pools (both non-null, as in
+ * paged_attention_append_decode_fp8 / paged_attention_decode_fp8).  `plan`
+ * must come from paged_attention_plan with the same block_tables, seq_lens,
+ * positions (null or not) and sizes; a plan made for a different launch size
+ * sets PKV_DEV_ERR_PLAN and the call writes nothing.  Workspace as for
+ * paged_attention_decode.  Supported for the staged kernel's shapes
+ * (paged_attention_plan_size(...) > 0); PKV_ERR_UNSUPPORTED otherwise.
+ *
+ * flags: 0 or PKV_FLAG_PDL, as for paged_attention_append_decode; a PDL launch
+ * also reads the plan before the preceding kernel completes, so the plan must
+ * not be written by that kernel: launch the step's first planned call after
+ * paged_attention_plan without PKV_FLAG_PDL (or with other work in between).
+ */
+int paged_attention_decode_planned(void* out, const void* q, void* k_pool, void* v_pool,
+                                   const float* k_scale, const float* v_scale,
+                                   const int32_t* block_tables, const int32_t* seq_lens,
+                                   const int32_t* positions, const void* k_new, const void* v_new,
+                                   int rows, int q_heads, int kv_heads, int head_dim,
+                                   int block_size, float scale, int max_blocks_per_row,
+                                   int num_blocks, int max_seq_len, const void* plan,
+                                   size_t plan_bytes, void* workspace, size_t workspace_bytes,
+                                   unsigned flags, int32_t* dev_err, cudaStream_t stream);
 
 /* Bytes of the static device scratch behind paged_attention_decode_noalloc
  * (8 MiB, held by every GPU that loads the library until the process exits). */

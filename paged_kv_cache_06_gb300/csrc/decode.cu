@@ -390,3 +390,71 @@ extern "C" int paged_attention_append_decode(
                                   num_blocks, max_seq_len, workspace, workspace_bytes, dev_err,
                                   stream);
 }
+
+extern "C" size_t paged_attention_plan_size(int rows, int q_heads, int kv_heads, int head_dim,
+                                            int max_seq_len, int block_size) {
+    using namespace pkv;
+    if (check_heads(q_heads, kv_heads, head_dim) != PKV_OK || rows <= 0 || max_seq_len < 0 ||
+        block_size <= 0 || !tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size))
+        return 0;
+    return tma_plan_bytes(rows, kv_heads, max_seq_len);
+}
+
+extern "C" int paged_attention_plan(void* plan, size_t plan_bytes, const int32_t* block_tables,
+                                    const int32_t* seq_lens, const int32_t* positions, int rows,
+                                    int q_heads, int kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_row, int num_blocks, int max_seq_len,
+                                    int32_t* dev_err, cudaStream_t stream) {
+    using namespace pkv;
+    const int hs = check_heads(q_heads, kv_heads, head_dim);
+    if (hs != PKV_OK) return hs;
+    if (rows < 0 || block_size <= 0 || block_size > 1024 || max_blocks_per_row <= 0 ||
+        num_blocks <= 0 || max_seq_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_row * block_size) return PKV_ERR_INVALID_ARG;
+    if (!tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size))
+        return PKV_ERR_UNSUPPORTED;
+    if (rows == 0) return PKV_OK;
+    if (!plan || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(plan)) return PKV_ERR_INVALID_ARG;
+    if (plan_bytes < tma_plan_bytes(rows, kv_heads, max_seq_len)) return PKV_ERR_WORKSPACE;
+    return tma_plan_launch(plan, plan_bytes, block_tables, seq_lens, positions, rows, q_heads,
+                           kv_heads, block_size, max_blocks_per_row, num_blocks, max_seq_len,
+                           dev_err, stream);
+}
+
+extern "C" int paged_attention_decode_planned(
+    void* out, const void* q, void* k_pool, void* v_pool, const float* k_scale,
+    const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens,
+    const int32_t* positions, const void* k_new, const void* v_new, int rows, int q_heads,
+    int kv_heads, int head_dim, int block_size, float scale, int max_blocks_per_row,
+    int num_blocks, int max_seq_len, const void* plan, size_t plan_bytes, void* workspace,
+    size_t workspace_bytes, unsigned flags, int32_t* dev_err, cudaStream_t stream) {
+    using namespace pkv;
+    const int hs = check_heads(q_heads, kv_heads, head_dim);
+    if (hs != PKV_OK) return hs;
+    if (rows < 0 || block_size <= 0 || block_size > 1024 || max_blocks_per_row <= 0 ||
+        num_blocks <= 0 || max_seq_len < 0 || !isfinite(scale) || (flags & ~PKV_FLAG_PDL))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_seq_len > (int64_t)max_blocks_per_row * block_size) return PKV_ERR_INVALID_ARG;
+    const bool fp8 = k_scale != nullptr || v_scale != nullptr;
+    if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (!tma_decode_supported(rows, q_heads, kv_heads, head_dim, block_size) ||
+        (fp8 && kv_heads > 16))
+        return PKV_ERR_UNSUPPORTED;
+    if (rows == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !plan)
+        return PKV_ERR_INVALID_ARG;
+    if (positions && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(plan) || (positions && (!aligned16(k_new) || !aligned16(v_new))))
+        return PKV_ERR_INVALID_ARG;
+    if (plan_bytes < tma_plan_bytes(rows, kv_heads, max_seq_len)) return PKV_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < tma_workspace_bytes(rows, q_heads, kv_heads, max_seq_len))
+        return PKV_ERR_WORKSPACE;
+    const AppendArgs app{positions, k_new, v_new};
+    return tma_decode_launch(out, q, k_pool, v_pool, block_tables, seq_lens, rows, q_heads,
+                             kv_heads, block_size, scale, max_blocks_per_row, num_blocks,
+                             max_seq_len, 0, workspace, dev_err, stream, positions ? &app : nullptr,
+                             (flags & PKV_FLAG_PDL) != 0, k_scale, v_scale, plan);
+}

@@ -12,26 +12,25 @@
 // granules.  All granules of all units, in (row, head, token) order, are cut
 // into gridDim.x equal contiguous ranges, one per thread block (one block per
 // SM), so every SM moves the same number of bytes whatever the length mix.
-// Each block derives the partition itself from seq_lens (a block-wide scan),
-// so the host never reads device lengths.  The part of a unit inside one
-// block is a piece.  A unit with pieces in several blocks is merged by the
-// block that holds its last piece: every piece publishes a partial record
-// (running max, sum and unnormalised output) and counts itself on a per-unit
-// counter with a release; the merging block waits (bounded) until the others
-// have all counted, lands every record and combines them through their
-// log-sum-exp, then re-arms the counter.  A block merges at most one unit.
+// The host never reads device lengths: the split of a step (each block's
+// range, pieces, warp shares and the physical rows of its granules) is a
+// plan, made on the device from seq_lens and the block tables, either by
+// each block in its prologue or once per step by paged_attention_plan for
+// all the layers of the step.  The part of a unit inside one block is a
+// piece.
 //
-// Block layout.  Warp 4 is the producer: it resolves each granule's physical
+// Block layout.  Warp 7 is the producer: it resolves each granule's physical
 // block from the table and issues TMA tiled copies (a 16-token x 64-dim box,
 // 128-byte swizzle, never crossing a physical block) into a ring of twelve
-// 8 KB granule slots.  Warps 0-3 consume, in one of two modes:
+// 8 KB granule slots.  Warps 0-6 consume, in one of two modes:
 //   * burst: the block's whole range fits the ring and covers at most four
-//     pieces.  Every copy is issued before the dependency wait, warps are
-//     dealt to pieces in proportion to their size, and each warp attends to
-//     its granules; the warps' partial states are then combined for all
-//     pieces together.
+//     pieces.  Every copy is issued before the dependency wait, the seven
+//     warps are dealt to pieces in proportion to their size, and each warp
+//     attends to its granules; each piece's first warp then absorbs the
+//     states of the piece's other warps.
 //   * stream: the ring runs as three stages of four granules, one granule
-//     per warp per stage, and pieces are combined as they end.
+//     per warp (warps 0-3) per stage, and warp 0 absorbs the others' states
+//     as each piece ends.
 // Per granule (16 tokens) and group of query heads (up to 8):
 //   S^T[16 tok][8 heads] = K[16 tok][128] . Q^T        (mma.sync m16n8k16)
 //   online softmax per head in fp32, base-2 exponent
@@ -40,9 +39,27 @@
 // The grouped query heads are the MMA's N = 8 columns, so every K and V byte
 // is read once and feeds all heads of its group.
 //
+// A warp's softmax state is kept, dumped and published in the MMA fragment
+// layout: per lane the running max and sum of heads 2t, 2t+1 (t = lane % 4)
+// and eight float4 chunks, chunk c holding O^T rows 16c + lane/4 and
+// 16c + 8 + lane/4 of those heads.  Chunk c of all lanes (512 bytes) is the
+// output's dims 16c..16c+15 for every head of the group.
+//
+// Split units.  A unit with pieces in P > 1 blocks is merged in slices: the
+// unit's first K = min(P, 8) pieces are its participants, participant k
+// merging the chunks c with c % K == k.  Every piece writes its combined
+// state as a record into the unit's region of the workspace (chunk-major
+// over the unit's pieces, so a participant's slice of all P records is
+// contiguous) and counts itself, with a release, on each participant's own
+// arrival counter.  A participant waits (bounded) until its counter reaches
+// P, re-arms it, lands its slice of the P records in the idle ring with one
+// bulk copy per chunk and merges them through their log-sum-exp in piece
+// order, so the result never depends on timing.
+//
 // Safety: table entries are range-checked before any copy is issued (a bad
-// entry is skipped and flagged); every mbarrier wait is bounded and a timeout
-// sets PKV_DEV_ERR_TIMEOUT, stops the block and drains its copies in flight.
+// entry is skipped and flagged); every mbarrier wait and counter poll is
+// bounded and a timeout sets PKV_DEV_ERR_TIMEOUT, stops the block and drains
+// its copies in flight.
 #include <cuda.h>
 
 #include <mutex>
@@ -55,34 +72,42 @@ namespace pkv {
 namespace tma {
 
 constexpr int kGranule = 16;        // tokens per box and per consumer warp step
-constexpr int kTileGranules = 4;    // stream mode: granules per stage (one per consumer warp)
+constexpr int kTileGranules = 4;    // stream mode: granules per stage (one per stream warp)
 constexpr int kStages = 3;
 constexpr int kRing = kStages * kTileGranules;  // granule slots
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 7;   // burst mode
+constexpr int kStreamWarps = 4;     // stream mode: warps 0-3 consume, 4-6 leave
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kMaxRows = 1024;
-constexpr int kRecHead = 16;   // per record: m[8], l[8], then o[group][128]
 constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
-constexpr int kMergeBatch = 8; // children merged per register batch
-constexpr int kMergeBars = 4;  // landing barriers, one per batch
-constexpr int kLandMax = kMergeBars * kMergeBatch;  // most records a landed merge takes
 constexpr int kBurstPieces = 4;
-constexpr int kBatch = 1;      // burst mode: granules per attend step (larger batches measured slower)
-constexpr int kCounterStride = 32;  // ints between the arrival counters of two units
-constexpr uint32_t kPollLimit = 1u << 21;  // polls of a merge wait (about a second)
+constexpr int kMaxTasks = 2;   // split pieces of a block: its first and its last
+constexpr int kMergeWays = 8;  // most participants of a split unit's merge
+constexpr uint32_t kPollLimit = 1u << 22;  // polls of a record batch (well over a second)
 constexpr uint32_t kBoxBytes = kGranule * 128;   // 16 rows x 128 B (64 dims)
 constexpr uint32_t kSlotBytes = 4 * kBoxBytes;   // K dims 0-63, K 64-127, V 0-63, V 64-127
 constexpr uint32_t kSlotV = 2 * kBoxBytes;
+constexpr uint32_t kChunkBytes = 512;            // one chunk of a state: 32 lanes x float4
+constexpr uint32_t kMlBytes = 64;                // m[8], l[8]
+constexpr uint32_t kStateBytes = kMlBytes + 8 * kChunkBytes;  // a dumped state
+constexpr uint32_t kLandBytes = kRing * kSlotBytes / kMaxTasks;  // merge partials per task
+constexpr int kModeIdle = 0, kModeBurst = 1, kModeStream = 2;
+constexpr uint32_t kPlanBytes = 512;             // one block's plan
+constexpr int kPlanThreads = 1024;               // threads of the plan kernel
 constexpr int kFp8MaxKvHeads = 16;                // FP8 pools: per-head scales kept in shared memory
 constexpr uint32_t kQBytes = 8 * 256;            // up to 8 query heads x 128 dims
-constexpr int kCombStride = 68;                  // stream combine: 64 dims + 4 pad (floats)
-constexpr int kDumpStride = 132;                 // burst dump: 128 dims + 4 pad (floats)
 constexpr float kLog2e = 1.4426950408889634f;
 
+// named barriers (0 is __syncthreads)
+constexpr int kBarConsumers = 1;  // burst: the seven consumer warps
+constexpr int kBarStream = 2;     // stream: warps 0-3
+constexpr int kBarPiece = 4;      // burst: 4 + piece, the piece's warps
+constexpr int kBarMerge = 8;      // 8 + task, the task's warps
+
 static_assert(kSlotBytes % 1024 == 0, "slots must keep 1024-byte alignment for 128B swizzle");
-static_assert((kRecHead + 8 * kDumpStride) * 4 <= (int)kSlotBytes, "a dumped partial fits one slot");
+static_assert(kStateBytes <= kSlotBytes, "a dumped state fits one slot");
 
 struct Params {
     __half* out;
@@ -93,9 +118,9 @@ struct Params {
     int limit;      // largest valid seq_len (paged); width (padded)
     int width;      // padded comparator: columns per row (0 = paged)
     float scale_log2;
-    int rec_floats; // floats per record: 16 + group * 128
-    int* counters;  // [units][kCounterStride]: pieces arrived per split unit (zero between calls)
-    float* records; // [slots][rec_floats]: partial results of split units
+    uint32_t poll_limit;  // polls of a record batch before a merge gives up
+    const unsigned char* plan;  // [grid][kPlanBytes] step plan, or null: each block makes its own
+    unsigned char* records;  // unit regions of split-piece records (zero between calls)
     int32_t* dev_err;
     // fused append (all null when the kernel only decodes)
     const int32_t* positions;
@@ -108,29 +133,45 @@ struct Params {
     const float* v_scale;
 };
 
-// Burst-mode plan of one block, written by thread 0 after the prologue.
-struct Plan {
-    int burst, npieces;
-    int r[kBurstPieces], kvh[kBurstPieces], ustart[kBurstPieces], n[kBurstPieces];
-    int P[kBurstPieces], cstart[kBurstPieces], w0[kBurstPieces], wn[kBurstPieces];
-    int wpiece[kConsumerWarps], wa[kConsumerWarps], wb[kConsumerWarps];
-    int valid[kRing];
+// A split piece of this block: its unit, the unit's first block and piece
+// count, this piece's index among them, and the unit's row and head.
+struct Task {
+    int u, cs, P, idx, r, kvh;
 };
+
+// One block's plan.  Burst blocks get their slots (physical row of each
+// granule's first token, or -1 for no copy; KV head; valid tokens), pieces
+// (row, head, unit's first granule, blocks holding the unit and the first of
+// them, first granule and size in this block, the appended token's unit-local
+// index when it falls in the piece), the warps dealt to each piece with their
+// granule ranges, and the split pieces as merge tasks.  Other blocks only get
+// their mode and range.
+struct BlockPlan {
+    int mode, g0, g1, G;  // G: the grid the plan was made for
+    int npieces, ntasks, W, Geff;
+    int pr[kBurstPieces], pkvh[kBurstPieces], pus[kBurstPieces], pP[kBurstPieces];
+    int pcs[kBurstPieces], pw0[kBurstPieces], pwn[kBurstPieces], ppatch[kBurstPieces];
+    int pfirst[kBurstPieces], psize[kBurstPieces];
+    int wpiece[8], wa[8], wb[8];
+    int szrow[kRing], skvh[kRing], svalid[kRing];
+    Task tasks[kMaxTasks];
+    int pad[8];
+};
+static_assert(sizeof(BlockPlan) == kPlanBytes, "a plan is 32 lanes x 16 bytes");
+static_assert(kConsumerWarps <= 8, "warp shares fit the plan");
 
 // Shared memory carve-up (offsets from a 1024-aligned base).
 struct Smem {
     static constexpr uint32_t ring = 0;
     static constexpr uint32_t q = ring + kRing * kSlotBytes;                        // [stages] stream queries
-    static constexpr uint32_t comb = q + kStages * kQBytes;                         // [4][8][68] f32
-    static constexpr uint32_t ml = comb + kConsumerWarps * 8 * kCombStride * 4;     // [4][8] m, [4][8] l
-    static constexpr uint32_t bars = ml + 2 * kConsumerWarps * 8 * 4;               // full[S], empty[S], slot[R], merge
-    static constexpr uint32_t desc = bars + (2 * kStages + kRing + 1 + kMergeBars) * 8;  // TileDesc[S]
-    static constexpr uint32_t plan = desc + kStages * 64;
-    static constexpr uint32_t flags = plan + ((sizeof(Plan) + 15) / 16) * 16;       // misc ints
+    static constexpr uint32_t bars = q + kStages * kQBytes;                         // full[S], empty[S], slot[R]
+    static constexpr uint32_t desc = bars + (2 * kStages + kRing) * 8;             // TileDesc[S]
+    static constexpr uint32_t plan = desc + kStages * 64;                           // BlockPlan
+    static constexpr uint32_t flags = plan + kPlanBytes;                            // misc ints
     static constexpr uint32_t scales = flags + 16 * 4;                              // FP8: k, v scale [2][16]
     static constexpr uint32_t ppos = scales + 2 * kFp8MaxKvHeads * 4;               // piece positions [32]
-    static constexpr uint32_t part = comb;  // scan partials: prologue only, aliases comb
-    static constexpr uint32_t prefix = ppos + kMaxPieces * 4;                       // rows + 1 ints
+    static constexpr uint32_t part = ppos + kMaxPieces * 4;                         // scan partials [kThreads]
+    static constexpr uint32_t prefix = part + kThreads * 4;                         // rows + 1 ints
     __host__ __device__ static constexpr uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
     __host__ __device__ static constexpr uint32_t total(int rows) { return lens(rows) + (uint32_t)rows * 4 + 1024; }
 };
@@ -143,8 +184,11 @@ static_assert(Smem::total(32) + 1024 <= 233472 / 2, "two blocks per SM at 32 row
 
 using namespace ptx;
 
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
 // Stream-mode tile descriptor: written by the producer before the stage's
@@ -179,6 +223,7 @@ __device__ __forceinline__ int owner_of(int g, int W, int G) {
 
 // Running softmax state of one warp: per lane, heads 2tq and 2tq+1
 // (tq = lane & 3) and the O^T fragments of all eight 16-dim row groups.
+// l0 / l1 are per-lane partial sums until reduce_l() folds the lanes.
 struct Soft {
     float m0, m1, l0, l1;
     float o[8][4];
@@ -188,53 +233,45 @@ struct Soft {
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
+    // sums over the eight lanes sharing tq (the token rows of a fragment)
+    __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+    }
 };
 
-// One online-softmax step of a warp over kB granules staged in slots
-// slot[0..kB-1] (K dims 0-63 at +0, K 64-127 at +2 KB, V at +4 KB / +6 KB,
-// 128-byte swizzled rows), valid[j] tokens each.  Rows past valid[j] must
-// hold finite values (zeroed by the caller) so that 0 * V stays 0.
-template <int kB>
-__device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], const uint32_t* slot,
-                                       const int* valid, float scale_log2, int lane) {
+// One online-softmax step of a warp over the granule staged at `slot` (K dims
+// 0-63 at +0, K 64-127 at +2 KB, V at +4 KB / +6 KB, 128-byte swizzled rows)
+// with `valid` tokens.  Rows past `valid` must hold finite values (zeroed by
+// the caller) so that 0 * V stays 0.
+__device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint32_t slot, int valid,
+                                       float scale_log2, int lane) {
     const int gq = lane >> 2;
-    float s[kB][4];
+    float s[4];
     {
-        // S^T = K . Q^T; per granule two independent chains (even / odd k-steps)
+        // S^T = K . Q^T; two independent chains (even / odd k-steps)
         const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-        float c0[kB][4], c1[kB][4];
-#pragma unroll
-        for (int j = 0; j < kB; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) c0[j][i] = c1[j][i] = 0.f;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const int chunk = (ks & 3) * 2 + (lane >> 4);
             const uint32_t off = (ks >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-#pragma unroll
-            for (int j = 0; j < kB; ++j) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(slot[j] + off, a0, a1, a2, a3);
-                mma16816((ks & 1) ? c1[j] : c0[j], a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
-            }
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(slot + off, a0, a1, a2, a3);
+            mma16816((ks & 1) ? c1 : c0, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
         }
 #pragma unroll
-        for (int j = 0; j < kB; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s[j][i] = c0[j][i] + c1[j][i];
+        for (int i = 0; i < 4; ++i) s[i] = c0[i] + c1[i];
     }
     // scores: s0 = (tok gq, head 2tq), s1 = (gq, 2tq+1), s2/3 = tok gq+8
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-        const int v = valid[j];
-        s[j][0] = gq < v ? s[j][0] * scale_log2 : -INFINITY;
-        s[j][1] = gq < v ? s[j][1] * scale_log2 : -INFINITY;
-        s[j][2] = gq + 8 < v ? s[j][2] * scale_log2 : -INFINITY;
-        s[j][3] = gq + 8 < v ? s[j][3] * scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
-        mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
-    }
+    s[0] = gq < valid ? s[0] * scale_log2 : -INFINITY;
+    s[1] = gq < valid ? s[1] * scale_log2 : -INFINITY;
+    s[2] = gq + 8 < valid ? s[2] * scale_log2 : -INFINITY;
+    s[3] = gq + 8 < valid ? s[3] * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -246,23 +283,15 @@ __device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], const
     const float al0 = fast_exp2(st.m0 - mu0), al1 = fast_exp2(st.m1 - mu1);
     st.m0 = mn0;
     st.m1 = mn1;
-    uint32_t pb0[kB], pb1[kB];
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-        const uint32_t px = pack_half2(fast_exp2(s[j][0] - mu0), fast_exp2(s[j][1] - mu1));
-        const uint32_t py = pack_half2(fast_exp2(s[j][2] - mu0), fast_exp2(s[j][3] - mu1));
-        // the sum takes the fp16 weights the MMA multiplies by
-        const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&px));
-        const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&py));
-        ls0 += fx.x + fy.x;
-        ls1 += fx.y + fy.y;
-        // B fragments of P^T (token x head) by transposing in registers
-        pb0[j] = movmatrix_t(px);
-        pb1[j] = movmatrix_t(py);
-    }
-    st.l0 = st.l0 * al0 + ls0;
-    st.l1 = st.l1 * al1 + ls1;
+    const uint32_t px = pack_half2(fast_exp2(s[0] - mu0), fast_exp2(s[1] - mu1));
+    const uint32_t py = pack_half2(fast_exp2(s[2] - mu0), fast_exp2(s[3] - mu1));
+    // the sum takes the fp16 weights the MMA multiplies by
+    const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&px));
+    const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&py));
+    st.l0 = st.l0 * al0 + (fx.x + fy.x);
+    st.l1 = st.l1 * al1 + (fx.y + fy.y);
+    // B fragments of P^T (token x head) by transposing in registers
+    const uint32_t pb0 = movmatrix_t(px), pb1 = movmatrix_t(py);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         st.o[i][0] *= al0;
@@ -276,12 +305,19 @@ __device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], const
     for (int mt = 0; mt < 8; ++mt) {
         const int chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
         const uint32_t off = kSlotV + (mt >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(slot + off, a0, a1, a2, a3);
+        mma16816(st.o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+}
+
+// Query fragments of heads kvh*group .. +7 of row r: b0 = Q[head gq][16ks + 2tq..],
+// b1 = Q[head gq][16ks + 8 + 2tq..] (heads past the group are zero).
+__device__ __forceinline__ void load_q(uint32_t (&qb)[16], const uint32_t* qrow, bool live, int tq) {
 #pragma unroll
-        for (int j = 0; j < kB; ++j) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(slot[j] + off, a0, a1, a2, a3);
-            mma16816(st.o[mt], a0, a1, a2, a3, pb0[j], pb1[j]);
-        }
+    for (int ks = 0; ks < 8; ++ks) {
+        qb[2 * ks] = live ? qrow[ks * 8 + tq] : 0u;
+        qb[2 * ks + 1] = live ? qrow[ks * 8 + 4 + tq] : 0u;
     }
 }
 
@@ -352,158 +388,548 @@ __device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
     __syncwarp();
 }
 
-// One batch of the log-sum-exp merge of P partial records (children j0 ..
-// j0 + kMergeBatch - 1 of P, rec_floats apart) for head mh, dims md..md+3 and
-// md+64..md+67, merged online: M is the running maximum of the children's m;
-// when a batch raises it, what is summed so far is scaled by 2^(M_old - M),
-// then L += 2^(m_j - M) l_j and o += 2^(m_j - M) o_j in child order, into two
-// accumulator sets (even / odd j) added at the end.  The arithmetic is the
-// same whether the records are read from shared or global memory, so the
-// result never depends on which block merges.  The sixteen threads of a head
-// read 256 contiguous bytes per load.
-template <bool kGlobal>
-__device__ __forceinline__ void merge_batch(const float* base, int j0, int P, int rec_floats, int mh,
-                                            int md, float& M, float& Ls, float& Ls2, float* acc,
-                                            float* acc2) {
-    auto ld1 = [&](const float* a) { return kGlobal ? __ldcg(a) : *a; };
-    auto ld4 = [&](const float* a) {
-        return kGlobal ? __ldcg(reinterpret_cast<const float4*>(a)) : *reinterpret_cast<const float4*>(a);
-    };
-    float w[kMergeBatch], l[kMergeBatch];
-    float4 x[kMergeBatch], y[kMergeBatch];
+// ---------------------------------------------------------------------------
+// States in the fragment layout: dump, output, records, merge.
+
+// Writes a warp's state (l reduced) at `dump`: per head pair tq one float4
+// (m[2tq], m[2tq+1], l[2tq], l[2tq+1]) at 16tq, then chunk c at 64 + 512c,
+// lane-major (conflict-free 16-byte stores).
+__device__ __forceinline__ void dump_state(const Soft& st, unsigned char* dump, int lane) {
+    if (lane < 4) *reinterpret_cast<float4*>(dump + 16 * lane) = make_float4(st.m0, st.m1, st.l0, st.l1);
 #pragma unroll
-    for (int c = 0; c < kMergeBatch; ++c) {  // a batch's loads are in flight together
-        if (j0 + c < P) {
-            const float* cr = base + (int64_t)(j0 + c) * rec_floats;
-            w[c] = ld1(cr + mh);
-            l[c] = ld1(cr + 8 + mh);
-            x[c] = ld4(cr + kRecHead + mh * kHeadDim + md);
-            y[c] = ld4(cr + kRecHead + mh * kHeadDim + md + 64);
-        } else {
-            w[c] = -INFINITY;
-            l[c] = 0.f;
-            x[c] = y[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    float Mb = M;
-#pragma unroll
-    for (int c = 0; c < kMergeBatch; ++c) Mb = fmaxf(Mb, w[c]);
-    if (Mb == -INFINITY) return;
-    if (Mb > M) {
-        const float sc = M == -INFINITY ? 0.f : fast_exp2(M - Mb);
-        Ls *= sc;
-        Ls2 *= sc;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            acc[i] *= sc;
-            acc2[i] *= sc;
-        }
-        M = Mb;
-    }
-#pragma unroll
-    for (int c = 0; c < kMergeBatch; c += 2) {
-        const float wa = fast_exp2(w[c] - M), wb = fast_exp2(w[c + 1] - M);
-        Ls += wa * l[c];
-        Ls2 += wb * l[c + 1];
-        acc[0] += wa * x[c].x; acc[1] += wa * x[c].y; acc[2] += wa * x[c].z; acc[3] += wa * x[c].w;
-        acc[4] += wa * y[c].x; acc[5] += wa * y[c].y; acc[6] += wa * y[c].z; acc[7] += wa * y[c].w;
-        acc2[0] += wb * x[c + 1].x; acc2[1] += wb * x[c + 1].y; acc2[2] += wb * x[c + 1].z;
-        acc2[3] += wb * x[c + 1].w; acc2[4] += wb * y[c + 1].x; acc2[5] += wb * y[c + 1].y;
-        acc2[6] += wb * y[c + 1].z; acc2[7] += wb * y[c + 1].w;
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(dump + kMlBytes + c * kChunkBytes + lane * 16) =
+            make_float4(st.o[c][0], st.o[c][1], st.o[c][2], st.o[c][3]);
+}
+
+// Stores chunk c (dims 16c..16c+15) of a normalised state as fp16 into the
+// group's output rows `ob` (head h at ob + 128h).  movmatrix turns the
+// (dim, head-pair) fragment into (head, dim-pair) words.
+__device__ __forceinline__ void store_chunk(__half* ob, int c, const float (&o)[4], float inv0,
+                                            float inv1, int group, int lane) {
+    const uint32_t x = movmatrix_t(pack_half2(o[0] * inv0, o[1] * inv1));
+    const uint32_t y = movmatrix_t(pack_half2(o[2] * inv0, o[3] * inv1));
+    const int h = lane >> 2, d = 16 * c + 2 * (lane & 3);
+    if (h < group) {
+        *reinterpret_cast<uint32_t*>(ob + h * kHeadDim + d) = x;
+        *reinterpret_cast<uint32_t*>(ob + h * kHeadDim + d + 8) = y;
     }
 }
 
-// Burst plan for the block's range [g0, g1): its pieces (at most four) and
-// the warps dealt to them.  Every piece gets one warp; each further warp goes
-// to the piece whose busiest warp has the most granules, while that is more
-// than one.  A piece's warps take near-equal contiguous shares of it.
-__device__ void make_plan(Plan& pl, volatile int* flags, const int* sm_pre, const int* sm_len, int rows,
-                          int hk, int g0, int g1, int W, int Geff) {
-    pl.burst = 0;
-    pl.npieces = 0;
-    for (int w = 0; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
-    if (g0 >= g1 || g1 - g0 > kRing) return;
-    int lo = 0, hi = rows - 1;
-    while (lo < hi) {  // largest row with sm_pre[row] <= g0
-        const int mid = (lo + hi + 1) >> 1;
-        if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
+// ---------------------------------------------------------------------------
+// Split-unit records.  Every word of a record is 8 bytes: a float's bits in
+// the low half and a flag (1) in the high half.  Naturally aligned 8-byte
+// relaxed accesses are single-copy atomic, so a reader that sees the flag
+// sees the value with it: the writer needs no fence or release and the
+// reader no separate arrival counter or second read.  The reader clears the
+// words it took, so the workspace is all zero between calls.
+//
+// Region of unit u (pieces in blocks cs .. cs+P-1) at slot cs + u: chunk c of
+// piece i at ((c*P + i)*32 + lane) * 32 bytes (the lane's four floats), then
+// m/l of piece i for participant k at 8*P*1 KB + (k*P + i)*128 + tq*32
+// (m[2tq], m[2tq+1], l[2tq], l[2tq+1]).  Participant k reads chunks
+// c = k, k + K, ... of every piece and its own m/l copies, so no word is
+// read by two blocks.
+constexpr uint32_t kLLChunk = 32 * 4 * 8;   // one chunk of a state as words: 1 KB
+constexpr uint32_t kLLMl = 4 * 4 * 8;       // m/l of one piece for one participant
+constexpr uint32_t kRecBytes = 8 * kLLChunk + kMergeWays * kLLMl;  // per record slot
+
+__device__ __forceinline__ unsigned char* unit_region(const Params& p, int u, int cs) {
+    return p.records + (int64_t)(cs + u) * kRecBytes;
+}
+__device__ __forceinline__ void st_words(unsigned char* a, float x, float y) {
+    const uint64_t w0 = (1ull << 32) | __float_as_uint(x), w1 = (1ull << 32) | __float_as_uint(y);
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(a), "l"(w0), "l"(w1) : "memory");
+}
+__device__ __forceinline__ void clear_words(unsigned char* a) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %1};" ::"l"(a), "l"(0ull) : "memory");
+}
+__device__ __forceinline__ void ld_words(const unsigned char* a, uint64_t& w0, uint64_t& w1) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a) : "memory");
+}
+__device__ __forceinline__ bool flagged(uint64_t w) { return (w >> 32) == 1u; }
+__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+
+// Where a piece's combined state goes: its unit's fp16 output rows (P == 1),
+// or its record (P > 1, piece idx of the unit, K participants).
+struct PieceOut {
+    __half* ob;             // output rows of the unit's query heads
+    unsigned char* region;  // the unit's record region
+    int P, idx, K, group;
+    float vs;               // FP8 V scale (1 for fp16 pools)
+};
+__device__ __forceinline__ PieceOut piece_out(const Params& p, int r, int kvh, int cs, int P, int cta,
+                                              float vs) {
+    PieceOut po;
+    po.ob = p.out + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim;
+    po.region = unit_region(p, r * p.hk + kvh, cs);
+    po.P = P;
+    po.idx = cta - cs;
+    po.K = P < kMergeWays ? P : kMergeWays;
+    po.group = p.group;
+    po.vs = vs;
+    return po;
+}
+
+// Chunk c of a piece's combined state (unnormalised acc, sums L0 / L1): the
+// fp16 output dims 16c.. when the unit is whole, else the record words.
+__device__ __forceinline__ void emit_chunk(const PieceOut& po, int c, const float (&acc)[4], float L0,
+                                           float L1, int lane) {
+    if (po.P == 1) {
+        const float inv0 = L0 > 0.f ? __fdividef(po.vs, L0) : 0.f;
+        const float inv1 = L1 > 0.f ? __fdividef(po.vs, L1) : 0.f;
+        store_chunk(po.ob, c, acc, inv0, inv1, po.group, lane);
+    } else {
+        unsigned char* a = po.region + (size_t)(c * po.P + po.idx) * kLLChunk + lane * 32;
+        st_words(a, acc[0], acc[1]);
+        st_words(a + 16, acc[2], acc[3]);
     }
-    int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-    int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n;
-    int k = 0;
-    for (int g = g0; g < g1;) {
-        if (k == kBurstPieces) return;  // too many pieces: stream mode
-        const int pend = min(g1, us + n);
-        pl.r[k] = r;
-        pl.kvh[k] = kvh;
-        pl.ustart[k] = us;
-        pl.n[k] = n;
-        pl.cstart[k] = owner_of(us, W, Geff);
-        pl.P[k] = owner_of(us + n - 1, W, Geff) - pl.cstart[k] + 1;
-        pl.w0[k] = g;  // piece range [w0, wn) until the warps are dealt below
-        pl.wn[k] = pend;
-        ++k;
-        g = pend;
-        if (g >= g1) break;
-        if (kvh + 1 < hk) {
-            ++kvh;
-            us += n;
-        } else {
-            ++r;
-            while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
-            kvh = 0;
-            n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-            us = sm_pre[r];
+}
+// m/l of a split piece, one copy per participant (lanes 0-3).
+__device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, float L0, float L1,
+                                        int lane) {
+    if (po.P == 1 || lane >= 4) return;
+#pragma unroll 1
+    for (int k = 0; k < po.K; ++k) {
+        unsigned char* a =
+            po.region + (size_t)8 * po.P * kLLChunk + (size_t)(k * po.P + po.idx) * kLLMl + lane * 32;
+        st_words(a, M0, M1);
+        st_words(a + 16, L0, L1);
+    }
+}
+
+// A piece held by one warp (l reduced): emits every chunk and the m/l.
+__device__ __forceinline__ void finish_own(const PieceOut& po, const Soft& st, int lane) {
+    if (po.P == 1) {
+        const float inv0 = st.l0 > 0.f ? __fdividef(po.vs, st.l0) : 0.f;
+        const float inv1 = st.l1 > 0.f ? __fdividef(po.vs, st.l1) : 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) store_chunk(po.ob, c, st.o[c], inv0, inv1, po.group, lane);
+        return;
+    }
+    unsigned char* a = po.region + (size_t)po.idx * kLLChunk + lane * 32;
+    const size_t step = (size_t)po.P * kLLChunk;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        st_words(a + c * step, st.o[c][0], st.o[c][1]);
+        st_words(a + c * step + 16, st.o[c][2], st.o[c][3]);
+    }
+    emit_ml(po, st.m0, st.m1, st.l0, st.l1, lane);
+}
+
+// Warp j of a piece's k warps (k <= kConsumerWarps), whose states are dumped
+// in ring slots (state s in slot wa[s] - base, or base + s when wa is null):
+// combines them through their log-sum-exp for chunks c = j, j + k, ... and
+// emits those; warp 0 also emits the m/l.  Every state's offset, maximum and
+// sum is loaded up front, the weights are computed once, and each chunk's k
+// loads are issued together, so the chains overlap.
+__device__ void combine_dumps(const PieceOut& po, const unsigned char* ring, const int* wa, int base,
+                              int k, int j, int lane) {
+    const int tq = lane & 3;
+    uint32_t off[kConsumerWarps];
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s)
+        off[s] = s < k ? (uint32_t)((wa ? wa[s] - base : base + s)) * kSlotBytes : 0u;
+    float4 ml[kConsumerWarps];
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s)
+        ml[s] = s < k ? *reinterpret_cast<const float4*>(ring + off[s] + 16 * tq)
+                      : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s) {
+        M0 = fmaxf(M0, ml[s].x);
+        M1 = fmaxf(M1, ml[s].y);
+    }
+    float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s) {  // ml[s].x / .y become the weights
+        ml[s].x = M0 == -INFINITY ? 0.f : fast_exp2(ml[s].x - M0);
+        ml[s].y = M1 == -INFINITY ? 0.f : fast_exp2(ml[s].y - M1);
+        L0 += ml[s].x * ml[s].z;
+        L1 += ml[s].y * ml[s].w;
+    }
+#pragma unroll 1
+    for (int c = j; c < 8; c += k) {
+        float4 v[kConsumerWarps];
+#pragma unroll
+        for (int s = 0; s < kConsumerWarps; ++s)
+            v[s] = s < k ? *reinterpret_cast<const float4*>(ring + off[s] + kMlBytes + c * kChunkBytes + lane * 16)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < kConsumerWarps; ++s) {
+            acc[0] += ml[s].x * v[s].x;
+            acc[1] += ml[s].y * v[s].y;
+            acc[2] += ml[s].x * v[s].z;
+            acc[3] += ml[s].y * v[s].w;
         }
+        emit_chunk(po, c, acc, L0, L1, lane);
     }
-    // wc counts the warps of each piece (registers: the loops are unrolled)
-    int wc[kBurstPieces] = {1, 1, 1, 1};
+    if (j == 0) emit_ml(po, M0, M1, L0, L1, lane);
+}
+
+// Merge of a split unit's slice by participant t.idx (< K): chunks
+// c_m = idx + m*K for m < nch.  The task's nw warps form min(nch, nw) chunk
+// groups of gsz = nw / groups warps; the warp of rank q in group g merges
+// chunks m = g, g + groups, ... over records j = q, q + gsz, ..., polled in
+// batches of four, each batch taken once all its words are flagged, absorbed
+// in order (online maximum) and cleared.  With gsz > 1 the group's partials
+// meet in shared memory at `part` after the task's barrier and rank 0
+// combines them in rank order; the result never depends on timing.
+// Returns false if a poll gave up.
+__device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsigned char* part,
+                           int bar_id, float vs, volatile int* fail, int lane) {
+    const int P = t.P;
+    const int K = P < kMergeWays ? P : kMergeWays;
+    if (t.idx >= K) return true;  // not a participant
+    const int nch = (kMergeWays - t.idx + K - 1) / K;
+    const int groups = nch < nw ? nch : nw;
+    const int gsz = nw / groups;
+    const int g = lw % groups, q = lw / groups;
+    const bool active = q < gsz;
+    const int tq = lane & 3;
+    unsigned char* reg = unit_region(p, t.u, t.cs);
+    unsigned char* mlb = reg + (size_t)8 * P * kLLChunk + (size_t)t.idx * P * kLLMl + tq * 32;
+    __half* ob = p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim;
+    bool ok = true;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int m = g; active && m < nch; m += groups) {
+        const int c = t.idx + m * K;
+        const unsigned char* cb = reg + (size_t)c * P * kLLChunk + lane * 32;
+        M0 = M1 = -INFINITY;
+        L0 = L1 = 0.f;
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll 1
+        for (int j0 = q; j0 < P && ok; j0 += 4 * gsz) {
+            uint64_t w[4][8];
+            bool got = false;
+#pragma unroll 1
+            for (uint32_t it = 0; it < p.poll_limit; ++it) {
+                bool all = true;
 #pragma unroll
-    for (int e = 1; e < kConsumerWarps; ++e) {
-        if (e < k) continue;
-        int best = -1, bc = 1;
+                for (int b = 0; b < 4; ++b) {
+                    const int j = j0 + b * gsz;
+                    if (j >= P) continue;
+                    ld_words(mlb + j * kLLMl, w[b][0], w[b][1]);
+                    ld_words(mlb + j * kLLMl + 16, w[b][2], w[b][3]);
+                    ld_words(cb + j * kLLChunk, w[b][4], w[b][5]);
+                    ld_words(cb + j * kLLChunk + 16, w[b][6], w[b][7]);
 #pragma unroll
-        for (int i = 0; i < kBurstPieces; ++i) {
-            if (i >= k) break;
-            const int c = (pl.wn[i] - pl.w0[i] + wc[i] - 1) / wc[i];
-            if (c > bc) {
-                bc = c;
-                best = i;
+                    for (int e = 0; e < 8; ++e) all &= flagged(w[b][e]);
+                }
+                if (__all_sync(0xffffffffu, all)) {
+                    got = true;
+                    break;
+                }
+            }
+            if (!got) {
+                ok = false;
+                break;
+            }
+            // the batch's maximum first, then one rescale of the running sums
+            // and independent weighted adds (records past P weigh nothing)
+            float N0 = M0, N1 = M1;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                if (j0 + b * gsz >= P) continue;
+                N0 = fmaxf(N0, word_value(w[b][0]));
+                N1 = fmaxf(N1, word_value(w[b][1]));
+            }
+            const float a0 = N0 == -INFINITY ? 0.f : fast_exp2(M0 - N0);
+            const float a1 = N1 == -INFINITY ? 0.f : fast_exp2(M1 - N1);
+            L0 *= a0;
+            L1 *= a1;
+            acc[0] *= a0;
+            acc[1] *= a1;
+            acc[2] *= a0;
+            acc[3] *= a1;
+            M0 = N0;
+            M1 = N1;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int j = j0 + b * gsz;
+                if (j >= P) continue;
+                const float b0 = N0 == -INFINITY ? 0.f : fast_exp2(word_value(w[b][0]) - N0);
+                const float b1 = N1 == -INFINITY ? 0.f : fast_exp2(word_value(w[b][1]) - N1);
+                L0 += word_value(w[b][2]) * b0;
+                L1 += word_value(w[b][3]) * b1;
+                acc[0] += word_value(w[b][4]) * b0;
+                acc[1] += word_value(w[b][5]) * b1;
+                acc[2] += word_value(w[b][6]) * b0;
+                acc[3] += word_value(w[b][7]) * b1;
+                // taken: clear the chunk words (read by this warp alone) for the
+                // next call; the m/l words are shared by the task's warps
+                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk);
+                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk + 16);
             }
         }
-#pragma unroll
-        for (int i = 0; i < kBurstPieces; ++i)
-            if (i == best) ++wc[i];
-    }
-    int w = 0;
-#pragma unroll
-    for (int i = 0; i < kBurstPieces; ++i) {
-        if (i >= k) break;
-        const int a = pl.w0[i], len = pl.wn[i] - a;
-        pl.w0[i] = w;
-        pl.wn[i] = wc[i];
-        for (int j = 0; j < wc[i]; ++j, ++w) {
-            pl.wpiece[w] = i;
-            pl.wa[w] = a + j * len / wc[i];
-            pl.wb[w] = a + (j + 1) * len / wc[i];
+        if (gsz == 1 && ok) {
+            const float inv0 = L0 > 0.f ? __fdividef(vs, L0) : 0.f;
+            const float inv1 = L1 > 0.f ? __fdividef(vs, L1) : 0.f;
+            store_chunk(ob, c, acc, inv0, inv1, p.group, lane);
         }
     }
-    for (; w < kConsumerWarps; ++w) pl.wpiece[w] = -1;
-    pl.npieces = k;
-    pl.burst = 1;
-    // the split pieces, recorded now for the tail (their unit, first block,
-    // pieces, row, head)
-    int ks = 0;
-    for (int i = 0; i < k; ++i) {
-        if (pl.P[i] == 1) continue;
-        flags[4 + 5 * ks] = pl.r[i] * hk + pl.kvh[i];
-        flags[5 + 5 * ks] = pl.cstart[i];
-        flags[6 + 5 * ks] = pl.P[i];
-        flags[7 + 5 * ks] = pl.r[i];
-        flags[8 + 5 * ks] = pl.kvh[i];
-        ++ks;
+    if (!ok && lane == 0) *fail = 1;
+    if (gsz > 1) {
+        // groups == nch here: each warp holds one chunk's partial
+        *reinterpret_cast<float4*>(part + lw * 1024 + lane * 16) = make_float4(M0, M1, L0, L1);
+        *reinterpret_cast<float4*>(part + lw * 1024 + 512 + lane * 16) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
-    flags[3] = ks;
+    named_sync(bar_id, nw * 32);
+    if (*fail) {
+        if (lane == 0 && lw == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+        return false;
+    }
+    // every warp of the task is past the m/l words: clear them for the next call
+#pragma unroll 1
+    for (int j = lw; j < P; j += nw) {
+        clear_words(mlb + j * kLLMl);
+        clear_words(mlb + j * kLLMl + 16);
+    }
+    if (gsz == 1 || q != 0) return true;
+    // the group's partials (at most kConsumerWarps), all loaded up front
+    float4 pm[kConsumerWarps], pv[kConsumerWarps];
+#pragma unroll
+    for (int r = 0; r < kConsumerWarps; ++r) {
+        const unsigned char* pw = part + (r * groups + g) * 1024 + lane * 16;
+        pm[r] = r < gsz ? *reinterpret_cast<const float4*>(pw) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+        pv[r] = r < gsz ? *reinterpret_cast<const float4*>(pw + 512) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float G0 = -INFINITY, G1 = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kConsumerWarps; ++r) {
+        G0 = fmaxf(G0, pm[r].x);
+        G1 = fmaxf(G1, pm[r].y);
+    }
+    float S0 = 0.f, S1 = 0.f, out4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kConsumerWarps; ++r) {
+        const float w0 = G0 == -INFINITY ? 0.f : fast_exp2(pm[r].x - G0);
+        const float w1 = G1 == -INFINITY ? 0.f : fast_exp2(pm[r].y - G1);
+        S0 += w0 * pm[r].z;
+        S1 += w1 * pm[r].w;
+        out4[0] += w0 * pv[r].x;
+        out4[1] += w1 * pv[r].y;
+        out4[2] += w0 * pv[r].z;
+        out4[3] += w1 * pv[r].w;
+    }
+    const float inv0 = S0 > 0.f ? __fdividef(vs, S0) : 0.f;
+    const float inv1 = S1 > 0.f ? __fdividef(vs, S1) : 0.f;
+    store_chunk(ob, t.idx + g * K, out4, inv0, inv1, p.group, lane);
+    return true;
+}
+
+// Granule prefix over rows, by all NT threads of a block: sm_pre[r] = first
+// granule of row r (its KV heads' granules in head order), sm_pre[rows] = W;
+// sm_len[r] = the row's tokens, clamped to the bound (a length outside
+// [0, limit] is flagged when `flag` is set).  Returns W.
+template <int NT>
+__device__ int scan_lengths(const Params& p, bool paged, int* sm_pre, int* sm_len, int* sm_part,
+                            bool flag) {
+    const int tid = threadIdx.x, lane = tid & 31, rows = p.rows;
+    const int per = (rows + NT - 1) / NT;
+    bool bad_len = false;
+    int sum = 0;
+    for (int i = 0; i < per; ++i) {
+        const int r = tid * per + i;
+        if (r < rows) {
+            int L = p.seq_lens[r];
+            if (L < 0 || L > p.limit) {
+                if (paged) bad_len = true;
+                L = L < 0 ? 0 : p.limit;
+            }
+            sm_len[r] = L;  // tokens that count (clamped)
+            const int c = p.hk * granules_of(paged ? L : p.width);
+            sm_pre[r] = c;
+            sum += c;
+        }
+    }
+    sm_part[tid] = sum;
+    if (bad_len && flag) flag_error(p.dev_err, PKV_DEV_ERR_SEQ_LEN);
+    __syncthreads();
+    if (tid < 32) {
+        constexpr int kPer = (NT + 31) / 32;
+        int v[kPer];
+        int acc = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int idx = lane * kPer + j;
+            v[j] = idx < NT ? sm_part[idx] : 0;
+            acc += v[j];
+        }
+        int incl = acc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int run = incl - acc;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int idx = lane * kPer + j;
+            if (idx < NT) sm_part[idx] = run;
+            run += v[j];
+        }
+    }
+    __syncthreads();
+    {
+        int run = sm_part[tid];
+        for (int i = 0; i < per; ++i) {
+            const int r = tid * per + i;
+            if (r < rows) {
+                const int c = sm_pre[r];
+                sm_pre[r] = run;
+                run += c;
+            }
+        }
+        if (tid == NT - 1) sm_pre[rows] = run;
+    }
+    __syncthreads();
+    return sm_pre[rows];
+}
+
+// One warp writes block b's plan into bp (shared memory), from the granule
+// prefix of a scan_lengths.  The W granules are cut into Geff = min(G, W)
+// equal contiguous ranges; block b's range is burst when it fits the ring
+// and covers at most four pieces.  Lane j resolves granule g0 + j (row, KV
+// head, valid tokens, physical row through the table).  Every piece gets one
+// warp; each further warp goes to the piece whose busiest warp has the most
+// granules, while that is more than one, and a piece's warps take near-equal
+// contiguous shares of it.
+__device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int b, int G, int W,
+                                 int Geff, const int* sm_pre, const int* sm_len, int lane) {
+    const int hk = p.hk, rows = p.rows;
+    int g0 = 0, g1 = 0;
+    if (b < Geff) {
+        g0 = (int)((int64_t)W * b / Geff);
+        g1 = (int)((int64_t)W * (b + 1) / Geff);
+    }
+    const int ng = g1 - g0;
+    const bool fits = ng > 0 && ng <= kRing;
+    int u = -1, r = 0, kvh = 0, n = 1, us = 0, valid = 0, zrow = -1;
+    if (fits && lane < ng) {
+        const int gg = g0 + lane;
+        int lo = 0, hi = rows - 1;
+        while (lo < hi) {  // largest row with sm_pre[row] <= gg
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
+        }
+        r = lo;
+        n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+        kvh = (gg - sm_pre[r]) / n;
+        us = sm_pre[r] + kvh * n;
+        u = r * hk + kvh;
+        const int tok = (gg - us) * kGranule;
+        valid = min(kGranule, sm_len[r] - tok);
+        if (valid < 0) valid = 0;
+        if (paged) {
+            const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
+            if (pb < 0 || pb >= p.nb) {
+                flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+                valid = 0;
+            } else {
+                zrow = pb * p.bs + tok % p.bs;
+            }
+        } else {
+            zrow = r * p.width + tok;  // the comparator reads every column
+        }
+    }
+    const int up = __shfl_up_sync(0xffffffffu, u, 1);
+    const unsigned starts = __ballot_sync(0xffffffffu, u >= 0 && (lane == 0 || u != up));
+    const int np = __popc(starts);
+    const int mode = ng <= 0 ? kModeIdle : (fits && np <= kBurstPieces) ? kModeBurst : kModeStream;
+    if (lane == 0) {
+        bp->mode = mode;
+        bp->g0 = g0;
+        bp->g1 = g1;
+        bp->G = G;
+        bp->W = W;
+        bp->Geff = Geff;
+        bp->npieces = mode == kModeBurst ? np : 0;
+        bp->ntasks = 0;
+    }
+    if (lane < 8) bp->wpiece[lane] = -1;
+    if (mode != kModeBurst) {
+        __syncwarp();
+        return;
+    }
+    if (lane < ng) {
+        bp->szrow[lane] = zrow;
+        bp->skvh[lane] = kvh;
+        bp->svalid[lane] = valid;
+    }
+    if (u >= 0 && ((starts >> lane) & 1u)) {
+        const int k = __popc(starts & ((1u << lane) - 1u));
+        const unsigned later = lane == 31 ? 0u : (starts >> (lane + 1));
+        const int end = later ? lane + __ffs(later) : ng;  // the next piece's first lane
+        const int cs = owner_of(us, W, Geff);
+        bp->pr[k] = r;
+        bp->pkvh[k] = kvh;
+        bp->pus[k] = us;
+        bp->pcs[k] = cs;
+        bp->pP[k] = owner_of(us + n - 1, W, Geff) - cs + 1;
+        bp->pfirst[k] = g0 + lane;
+        bp->psize[k] = end - lane;
+        int patch = -1;
+        if (paged && p.positions) {
+            const int pos = p.positions[r];
+            if (pos >= 0) {
+                const int pg = us + pos / kGranule;
+                if (pg >= g0 + lane && pg < g0 + end) patch = pos;
+            }
+        }
+        bp->ppatch[k] = patch;
+    }
+    __syncwarp();
+    // deal the consumer warps: lane k < np holds piece k
+    const int sz = lane < np ? bp->psize[lane] : 0;
+    int wc = lane < np ? 1 : 0;
+    for (int e = np; e < kConsumerWarps; ++e) {
+        const int c = lane < np ? (sz + wc - 1) / wc : 0;
+        int best = c;
+        best = max(best, __shfl_xor_sync(0xffffffffu, best, 1));
+        best = max(best, __shfl_xor_sync(0xffffffffu, best, 2));
+        best = __shfl_sync(0xffffffffu, best, 0);  // lanes 0-3 hold the pieces
+        if (best <= 1) break;
+        const unsigned who = __ballot_sync(0xffffffffu, lane < np && c == best);
+        if (lane == __ffs(who) - 1) ++wc;
+    }
+    int w0 = 0;
+#pragma unroll
+    for (int j = 0; j < kBurstPieces; ++j) {
+        const int wj = __shfl_sync(0xffffffffu, wc, j);
+        if (j < lane) w0 += wj;
+    }
+    if (lane < np) {
+        bp->pw0[lane] = w0;
+        bp->pwn[lane] = wc;
+        const int a = bp->pfirst[lane];
+        for (int j = 0; j < wc; ++j) {
+            bp->wpiece[w0 + j] = lane;
+            bp->wa[w0 + j] = a + j * sz / wc;
+            bp->wb[w0 + j] = a + (j + 1) * sz / wc;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        // split pieces: a contiguous range has at most two, its first and its last
+        int nt = 0;
+        for (int k = 0; k < np; ++k) {
+            if (bp->pP[k] == 1 || nt == kMaxTasks) continue;
+            Task& t = bp->tasks[nt++];
+            t.u = bp->pr[k] * hk + bp->pkvh[k];
+            t.cs = bp->pcs[k];
+            t.P = bp->pP[k];
+            t.idx = b - bp->pcs[k];
+            t.r = bp->pr[k];
+            t.kvh = bp->pkvh[k];
+        }
+        bp->ntasks = nt;
+    }
+    __syncwarp();
 }
 
 // Per-row work of block cta, done by its producer warp after the dependency
@@ -514,9 +940,11 @@ __device__ void make_plan(Plan& pl, volatile int* flags, const int* sm_pre, cons
 // the token from k_new / v_new directly, so the order of this store and that
 // copy does not matter.
 template <bool kFp8>
-__device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int lane) {
+__device__ void row_work(const Params& p, int cta, int G, int lane) {
+#pragma unroll 1
     for (int r = cta; r < p.rows; r += G) {
-        if (sm_pre[r + 1] == sm_pre[r])
+        if (p.seq_lens[r] <= 0)
+#pragma unroll 1
             for (int i = lane; i < p.hq * kHeadDim / 8; i += 32)
                 reinterpret_cast<uint4*>(p.out + (int64_t)r * p.hq * kHeadDim)[i] = make_uint4(0, 0, 0, 0);
         if (!p.positions) continue;
@@ -534,6 +962,7 @@ __device__ void row_work(const Params& p, const int* sm_pre, int cta, int G, int
         }
         const int vecs = p.hk * kHeadDim / 8;  // 8-element vectors per token and pool
         const int64_t dst = ((int64_t)pb * p.bs + pos % p.bs) * vecs;
+#pragma unroll 1
         for (int i = lane; i < 2 * vecs; i += 32) {
             const bool is_v = i >= vecs;
             const int j = is_v ? i - vecs : i;
@@ -556,16 +985,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    float* sm_comb = reinterpret_cast<float*>(smem + Smem::comb);
-    float* sm_m = reinterpret_cast<float*>(smem + Smem::ml);
-    float* sm_l = sm_m + kConsumerWarps * 8;
     const uint32_t bar_full = sbase + Smem::bars;
     const uint32_t bar_empty = bar_full + kStages * 8;
     const uint32_t bar_slot = bar_full + 2 * kStages * 8;
-    const uint32_t bar_merge = bar_slot + kRing * 8;
     int* sm_ppos = reinterpret_cast<int*>(smem + Smem::ppos);
     TileDesc* sm_desc = reinterpret_cast<TileDesc*>(smem + Smem::desc);
-    Plan* sm_plan = reinterpret_cast<Plan*>(smem + Smem::plan);
+    BlockPlan* bp = reinterpret_cast<BlockPlan*>(smem + Smem::plan);
     volatile int* sm_flags = reinterpret_cast<volatile int*>(smem + Smem::flags);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
     int* sm_pre = reinterpret_cast<int*>(smem + Smem::prefix);
@@ -578,161 +1003,79 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int G = gridDim.x;  // blocks launched; the partition uses Geff <= G
+    const int G = gridDim.x;
     const int cta = blockIdx.x;
     const int hk = p.hk;
     const int rows = p.rows;
 
-
-    if (warp == kConsumerWarps && lane == 0) {
-        // fetch the tensor-map descriptors now; the first copy would wait for them
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    // The next kernel in the stream (launched with programmatic stream
+    // serialization) may be scheduled as soon as every block has started:
+    // its blocks then take the SMs' second slots as the blocks of the kernel
+    // before this one leave, and prefetch their own work.  It waits for this
+    // grid to complete before touching anything this grid writes.
+    griddep_launch();
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            // fetch the tensor-map descriptors now; the first copy would wait for them
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+        }
+        // the step's plan for this block: one 16-byte load per lane
+        if (p.plan)
+            reinterpret_cast<uint4*>(bp)[lane] =
+                __ldg(reinterpret_cast<const uint4*>(p.plan + (size_t)cta * kPlanBytes) + lane);
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+            mbar_init(bar_empty + 8 * s, kStreamWarps);
         }
+#pragma unroll 1
         for (int s = 0; s < kRing; ++s) mbar_init(bar_slot + 8 * s, 1);
-        for (int b = 0; b < kMergeBars; ++b) mbar_init(bar_merge + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sm_flags[0] = 0;  // abort
-        sm_flags[3] = 0;  // split pieces recorded ([4..13]: their unit, first block, pieces, row, head)
+        sm_flags[4] = sm_flags[5] = 0;  // a merge task's poll gave up
     }
     if (kFp8 && tid < 2 * p.hk) sm_ks[tid < p.hk ? tid : kFp8MaxKvHeads + tid - p.hk] =
         tid < p.hk ? p.k_scale[tid] : p.v_scale[tid - p.hk];
-
-    // ---- granule prefix over rows: sm_pre[r] = first granule of row r ----
-    const int per = (rows + kThreads - 1) / kThreads;
-    bool bad_len = false;
-    int sum = 0;
-    for (int i = 0; i < per; ++i) {
-        const int r = tid * per + i;
-        if (r < rows) {
-            int L = p.seq_lens[r];
-            if (L < 0 || L > p.limit) {
-                if (kPaged) bad_len = true;
-                L = L < 0 ? 0 : p.limit;
-            }
-            sm_len[r] = L;  // tokens that count (clamped)
-            const int c = hk * granules_of(kPaged ? L : p.width);
-            sm_pre[r] = c;
-            sum += c;
-        }
-    }
-    sm_part[tid] = sum;
-    if (bad_len && cta == 0) flag_error(p.dev_err, PKV_DEV_ERR_SEQ_LEN);
-    __syncthreads();
-    if (warp == 0) {
-        constexpr int kPer = (kThreads + 31) / 32;
-        int v[kPer];
-        int acc = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int idx = lane * kPer + j;
-            v[j] = idx < kThreads ? sm_part[idx] : 0;
-            acc += v[j];
-        }
-        int incl = acc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        int run = incl - acc;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int idx = lane * kPer + j;
-            if (idx < kThreads) sm_part[idx] = run;
-            run += v[j];
-        }
-    }
-    __syncthreads();
-    {
-        int run = sm_part[tid];
-        for (int i = 0; i < per; ++i) {
-            const int r = tid * per + i;
-            if (r < rows) {
-                const int c = sm_pre[r];
-                sm_pre[r] = run;
-                run += c;
-            }
-        }
-        if (tid == kThreads - 1) sm_pre[rows] = run;
-    }
     __syncthreads();
 
-    // Partition over Geff = min(grid, W) blocks so every participating block
-    // owns at least one granule (a merge counts on one piece per block).
-    const int W = sm_pre[rows];
-    const int Geff = W < G ? W : G;
-    const int g0 = cta < Geff ? (int)((int64_t)W * cta / Geff) : 0;
-    const int g1 = cta < Geff ? (int)((int64_t)W * (cta + 1) / Geff) : 0;
+    // ---- the block's plan: loaded (made for this grid), or made here ----
+    int W, Geff;
+    if (p.plan) {
+        if (bp->G != G) {  // made for another grid: nothing is read or written
+            if (tid == 0) flag_error(p.dev_err, PKV_DEV_ERR_PLAN);
+            return;
+        }
+        W = bp->W;
+        Geff = bp->Geff;
+        // stream blocks walk their range through the granule prefix
+        if (bp->mode == kModeStream) scan_lengths<kThreads>(p, kPaged, sm_pre, sm_len, sm_part, false);
+    } else {
+        W = scan_lengths<kThreads>(p, kPaged, sm_pre, sm_len, sm_part, cta == 0);
+        Geff = W < G ? W : G;
+        if (warp == kConsumerWarps) build_block_plan(bp, p, kPaged, cta, G, W, Geff, sm_pre, sm_len, lane);
+        __syncthreads();
+    }
+    const int mode = bp->mode;
+    const int g0 = bp->g0, g1 = bp->g1;
 
     if (warp == kConsumerWarps) {
         // ============================ producer ============================
-        if (g0 >= g1) {
+        if (mode == kModeIdle) {
             griddep_wait();
-            if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
+            if (kPaged) row_work<kFp8>(p, cta, G, lane);
             return;
         }
-        // Burst mode when the range fits the ring and covers at most
-        // kBurstPieces units (the consumers' plan, made concurrently, takes
-        // the same decision).
-        bool burst = false;
-        if (g1 - g0 <= kRing) {
-            int u = -1;
-            if (lane < g1 - g0) {
-                const int gg = g0 + lane;
-                int lo = 0, hi = rows - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
-                }
-                const int n = (sm_pre[lo + 1] - sm_pre[lo]) / hk;
-                u = lo * hk + (gg - sm_pre[lo]) / n;
-            }
-            const int up = __shfl_up_sync(0xffffffffu, u, 1);
-            const int pieces = __popc(__ballot_sync(0xffffffffu, u >= 0 && (lane == 0 || u != up)));
-            burst = pieces <= kBurstPieces;
-        }
-        if (burst) {
+        if (mode == kModeBurst) {
             // Every granule of the range goes to its own slot now, before the
             // dependency wait; lane j handles granule g0 + j.
             const int ng = g1 - g0;
             if (lane < ng) {
-                const int gg = g0 + lane;
-                int lo = 0, hi = rows - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
-                }
-                const int r = lo;
-                const int n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                const int kvh = (gg - sm_pre[r]) / n;
-                const int tok = (gg - sm_pre[r] - kvh * n) * kGranule;
-                int valid = min(kGranule, sm_len[r] - tok);
-                if (valid < 0) valid = 0;
-                bool issue = false;
-                int zrow = 0;
-                if (kPaged) {
-                    const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
-                    if (pb < 0 || pb >= p.nb) {
-                        flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-                        valid = 0;
-                    } else {
-                        zrow = pb * p.bs + tok % p.bs;
-                        issue = true;
-                    }
-                } else {
-                    zrow = r * p.width + tok;
-                    issue = true;
-                }
-                sm_plan->valid[lane] = valid;
+                const int zrow = bp->szrow[lane], kvh = bp->skvh[lane];
                 const uint32_t fb = bar_slot + 8 * lane;
-                mbar_arrive_expect_tx(fb, issue ? kGranuleLoad : 0u);
-                if (issue) {
+                mbar_arrive_expect_tx(fb, zrow >= 0 ? kGranuleLoad : 0u);
+                if (zrow >= 0) {
                     const uint32_t dst = sbase + Smem::ring + lane * kSlotBytes;
                     if (kFp8) {
                         tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
@@ -746,8 +1089,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             griddep_wait();
-            if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
+            if (kPaged) row_work<kFp8>(p, cta, G, lane);
             // Drain: every copy lands before the block exits.
+#pragma unroll 1
             for (int j = 0; j < ng; ++j)
                 if (!mbar_wait(bar_slot + 8 * j, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
             return;
@@ -890,7 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
             }
         }
-        if (kPaged) row_work<kFp8>(p, sm_pre, cta, G, lane);
+        if (kPaged) row_work<kFp8>(p, cta, G, lane);
         // Drain: the copies of every armed stage land before the block exits.
         for (int t = tile - kStages; t < tile; ++t) {
             if (t < 0) continue;
@@ -901,15 +1245,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ============================== consumers ==============================
-    if (tid == 0) make_plan(*sm_plan, sm_flags, sm_pre, sm_len, rows, hk, g0, g1, W, Geff);
-    consumer_sync();
-    const bool burst = sm_plan->burst != 0;
-    if (burst && sm_plan->wpiece[warp] >= 0) {
+    const bool burst = mode == kModeBurst;
+    if (!burst && warp >= kStreamWarps) return;  // stream mode runs on warps 0-3
+    if (burst && bp->wpiece[warp] >= 0) {
         // Warm L2 with this warp's query rows and new token.  A prefetch reads
         // nothing into the block, so it may precede the dependency wait: the
         // values used are loaded after it.
-        const int pi = sm_plan->wpiece[warp];
-        const int r = sm_plan->r[pi], kvh = sm_plan->kvh[pi];
+        const int pi = bp->wpiece[warp];
+        const int r = bp->pr[pi], kvh = bp->pkvh[pi];
         const char* qrow = reinterpret_cast<const char*>(p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim);
         if (lane < 2 * p.group)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lane * 128));
@@ -918,14 +1261,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
             asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
         }
-        if (kPaged && p.positions && lane == 8)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.positions + r));
     }
     // Everything below may read what the preceding kernel wrote (query,
     // positions, new tokens, workspace) or write what it reads.
     griddep_wait();
 
-    if (g0 >= g1) return;
+    if (mode == kModeIdle) return;
 
     const bool fused = kPaged && p.positions != nullptr;
     const int gq = lane >> 2;  // MMA group id: token row (QK) / dim row (PV) / head (B frag)
@@ -933,176 +1274,79 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (burst) {
         // ============================ burst mode ============================
-        const Plan& pl = *sm_plan;
-        const int pi = pl.wpiece[warp];
+        const int pi = bp->wpiece[warp];
+        Soft st;
+        st.reset();
+        bool ok = true;
+        int r = 0, kvh = 0;
         if (pi >= 0) {
-            const int r = pl.r[pi], kvh = pl.kvh[pi], us = pl.ustart[pi];
-            const int a = pl.wa[warp], b = pl.wb[warp];
-            // Query fragments straight from global memory: b0 = Q[head gq][16ks + 2tq..],
-            // b1 = Q[head gq][16ks + 8 + 2tq..].
+            r = bp->pr[pi];
+            kvh = bp->pkvh[pi];
+            const int us = bp->pus[pi];
+            const int a = bp->wa[warp], b = bp->wb[warp];
             uint32_t qb[16];
-            {
-                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                    p.q + ((int64_t)r * p.hq + kvh * p.group + gq) * kHeadDim);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    qb[2 * ks] = gq < p.group ? qrow[ks * 8 + tq] : 0u;
-                    qb[2 * ks + 1] = gq < p.group ? qrow[ks * 8 + 4 + tq] : 0u;
-                }
-            }
+            load_q(qb, reinterpret_cast<const uint32_t*>(p.q + ((int64_t)r * p.hq + kvh * p.group + gq) * kHeadDim),
+                   gq < p.group, tq);
             // The appended token, if it falls inside this warp's granules, is
             // taken from k_new / v_new (its slot may be written concurrently).
             int patch_tok = -1;
             uint4 patch_val = make_uint4(0, 0, 0, 0);
-            if (fused) {
+            const int pos = fused ? bp->ppatch[pi] : -1;
+            if (pos >= 0 && us + pos / kGranule >= a && us + pos / kGranule < b) {
+                patch_tok = pos;
                 const uint4* src = reinterpret_cast<const uint4*>(
                     (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                 patch_val = src[lane & 15];
                 // FP8 pools hold the token as codes: take their exact fp16 values
                 if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
-                const int pos = p.positions[r];
-                if (pos >= 0 && us + pos / kGranule >= a && us + pos / kGranule < b) patch_tok = pos;
             }
-            Soft st;
-            st.reset();
-            bool ok = true;
-            for (int bs = a; bs < b && ok; bs += kBatch) {
-                const int nb = min(kBatch, b - bs);
-                uint32_t slot[kBatch];
-                int valid[kBatch];
+            const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
+#pragma unroll 1
+            for (int g = a; g < b; ++g) {
+                const int si = g - g0;
+                if (!mbar_wait(bar_slot + 8 * si, 0)) {
+                    if (lane == 0) {
+                        sm_flags[0] = 1;
+                        flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+                    }
+                    ok = false;
+                    break;
+                }
+                const int valid = bp->svalid[si];
+                unsigned char* sp = smem + Smem::ring + si * kSlotBytes;
                 bool wrote = false;
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    slot[j] = sbase;
-                    valid[j] = 0;
-                    if (j >= nb || !ok) continue;
-                    const int si = bs + j - g0;
-                    if (!mbar_wait(bar_slot + 8 * si, 0)) {
-                        if (lane == 0) {
-                            sm_flags[0] = 1;
-                            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                        }
-                        ok = false;
-                        continue;
-                    }
-                    slot[j] = sbase + Smem::ring + si * kSlotBytes;
-                    valid[j] = pl.valid[si];
-                    const int gtok = (bs + j - us) * kGranule;
-                    if (kFp8) {
-                        widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
-                        wrote = true;
-                    }
-                    wrote |= prepare_granule(smem + Smem::ring + si * kSlotBytes, valid[j],
-                                             patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
+                if (kFp8) {
+                    widen_fp8_slot(sp, lane);
+                    wrote = true;
                 }
-                if (!ok) break;
+                const int gtok = (g - us) * kGranule;
+                wrote |= prepare_granule(sp, valid, patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
                 if (wrote) __syncwarp();
-                const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
-                attend<1>(st, qb, slot, valid, sl2, lane);
+                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid, sl2, lane);
             }
-            // Dump the warp's state into its first slot: m[8], l[8], o[8][132].
+            st.reduce_l();
             __syncwarp();
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
-                st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+            // A piece of several warps: each dumps its state into its first
+            // slot, and after the piece's barrier each combines a share of
+            // the chunks of all of them.
+            const int k = bp->pwn[pi];
+            if (k > 1) {
+                if (ok) dump_state(st, smem + Smem::ring + (a - g0) * kSlotBytes, lane);
+                named_sync(kBarPiece + pi, k * 32);
             }
-            float* dump = reinterpret_cast<float*>(smem + Smem::ring + (a - g0) * kSlotBytes);
-            if (gq == 0) {
-                dump[2 * tq] = st.m0;
-                dump[2 * tq + 1] = st.m1;
-                dump[8 + 2 * tq] = st.l0;
-                dump[8 + 2 * tq + 1] = st.l1;
-            }
-            float* o0 = dump + kRecHead;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int dim = mt * 16 + gq;
-                o0[(2 * tq) * kDumpStride + dim] = st.o[mt][0];
-                o0[(2 * tq + 1) * kDumpStride + dim] = st.o[mt][1];
-                o0[(2 * tq) * kDumpStride + dim + 8] = st.o[mt][2];
-                o0[(2 * tq + 1) * kDumpStride + dim + 8] = st.o[mt][3];
-            }
-        }
-        consumer_sync();
-        // The next kernel in the stream (launched with programmatic
-        // serialization) may start now that this block's queries have
-        // arrived: its prefetch then no longer competes with them.  It waits
-        // for this grid before touching anything this grid writes.
-        if (tid == 0) griddep_launch();
-        if (sm_flags[0]) return;
-        // Combine every piece's warp states.  Thread (head h, dims 8c..8c+7)
-        // reads all four warps' states at once, then finishes each piece.
-        {
-            const int gsz = p.group;
-            const int h = tid >> 4, c = tid & 15;
-            float mw[kConsumerWarps], lw[kConsumerWarps];
-            float4 xw[kConsumerWarps], yw[kConsumerWarps];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                mw[w] = -INFINITY;
-                lw[w] = 0.f;
-                xw[w] = yw[w] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (pl.wpiece[w] >= 0 && h < gsz) {
-                    const float* dw = reinterpret_cast<const float*>(smem + Smem::ring +
-                                                                     (pl.wa[w] - g0) * kSlotBytes);
-                    mw[w] = dw[h];
-                    lw[w] = dw[8 + h];
-                    xw[w] = *reinterpret_cast<const float4*>(dw + kRecHead + h * kDumpStride + 8 * c);
-                    yw[w] = *reinterpret_cast<const float4*>(dw + kRecHead + h * kDumpStride + 8 * c + 4);
-                }
-            }
-            int pw0[kBurstPieces], pwn[kBurstPieces], pr[kBurstPieces], pkv[kBurstPieces], pP[kBurstPieces];
-#pragma unroll
-            for (int pc = 0; pc < kBurstPieces; ++pc) {
-                pw0[pc] = pl.w0[pc];
-                pwn[pc] = pl.wn[pc];
-                pr[pc] = pl.r[pc];
-                pkv[pc] = pl.kvh[pc];
-                pP[pc] = pl.P[pc];
-            }
-            const int npc = h < gsz ? pl.npieces : 0;
-#pragma unroll
-            for (int pc = 0; pc < kBurstPieces; ++pc) {
-                if (pc >= npc) break;
-                const int w0 = pw0[pc], w1 = w0 + pwn[pc];
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    if (w >= w0 && w < w1) M = fmaxf(M, mw[w]);
-                float L = 0.f, acc[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    if (w < w0 || w >= w1) continue;
-                    const float wt = M == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
-                    L += wt * lw[w];
-                    acc[0] += wt * xw[w].x; acc[1] += wt * xw[w].y; acc[2] += wt * xw[w].z; acc[3] += wt * xw[w].w;
-                    acc[4] += wt * yw[w].x; acc[5] += wt * yw[w].y; acc[6] += wt * yw[w].z; acc[7] += wt * yw[w].w;
-                }
-                const int r = pr[pc], kvh = pkv[pc];
-                if (pP[pc] == 1) {
-                    const float inv = L > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, L) : 0.f;
-                    uint4 pk;
-                    pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
-                    pk.y = pack_half2(acc[2] * inv, acc[3] * inv);
-                    pk.z = pack_half2(acc[4] * inv, acc[5] * inv);
-                    pk.w = pack_half2(acc[6] * inv, acc[7] * inv);
-                    *reinterpret_cast<uint4*>(p.out + ((int64_t)r * p.hq + kvh * gsz + h) * kHeadDim + 8 * c) = pk;
+            if (!sm_flags[0]) {
+                const int cs = bp->pcs[pi];
+                const PieceOut po = piece_out(p, r, kvh, cs, bp->pP[pi], cta, kFp8 ? sm_vs[kvh] : 1.f);
+                if (k == 1) {
+                    finish_own(po, st, lane);
                 } else {
-                    float* rec = p.records + (int64_t)(cta + r * hk + kvh) * p.rec_floats;
-                    if (c == 0) {
-                        rec[h] = M;
-                        rec[8 + h] = L;
-                    }
-                    *reinterpret_cast<float4*>(rec + kRecHead + h * kHeadDim + 8 * c) =
-                        make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    *reinterpret_cast<float4*>(rec + kRecHead + h * kHeadDim + 8 * c + 4) =
-                        make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    const int w0 = bp->pw0[pi];
+                    combine_dumps(po, smem + Smem::ring, bp->wa + w0, g0, k, warp - w0, lane);
                 }
             }
         }
+        // every dump has been read: the ring is free for the merges
+        named_sync(kBarConsumers, kConsumers);
     } else {
         // ============================ stream mode ============================
         // Append positions of this block's first pieces, read once right after
@@ -1133,7 +1377,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 sm_flags[2] = k;
             }
-            consumer_sync();
+            named_sync(kBarStream, kStreamWarps * 32);
         }
         // Each thread's position load stays in flight while the first tile lands;
         // it is published to shared memory after the first full barrier.
@@ -1160,7 +1404,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             if (!pos_published) {
                 if (tid < npp) sm_ppos[tid] = my_pos;
-                consumer_sync();
+                named_sync(kBarStream, kStreamWarps * 32);
                 pos_published = true;
             }
             const TileDesc* d = sm_desc + s;
@@ -1170,14 +1414,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int ustart = d->ustart, n = d->n, pend = d->pend;
             const int valid = warp < ng ? d->valid[warp] : 0;
             if (flags & kFirst) {
-                // B fragments of Q^T: b0 = Q[head gq][16ks + 2tq..], b1 = Q[head gq][16ks + 8 + 2tq..]
-                const uint32_t* qrow =
-                    reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    qb[2 * ks] = gq < p.group ? qrow[ks * 8 + tq] : 0u;
-                    qb[2 * ks + 1] = gq < p.group ? qrow[ks * 8 + 4 + tq] : 0u;
-                }
+                load_q(qb, reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256),
+                       gq < p.group, tq);
                 st.reset();
                 patch_tok = -1;
                 const int this_piece = piece++;
@@ -1196,216 +1434,96 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
+            bool wrote = false;
             if (warp < ng) {
                 const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
                 const int si = s * kTileGranules + warp;
                 if (kFp8) widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
-                const bool wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
-                                                   patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
+                wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
+                                               patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
                 if (wrote) __syncwarp();
-                const uint32_t slot[1] = {sbase + Smem::ring + si * kSlotBytes};
-                const int vv[1] = {valid};
-                attend<1>(st, qb, slot, vv, kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2, lane);
+                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid,
+                       kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2, lane);
+            }
+            ++tile;
+            if (!(flags & kLast)) {
                 // Generic-proxy writes must be ordered before TMA reuses the slot.
                 if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+                continue;
             }
+
+            // ---- end of a piece: the four warps dump their states into their
+            // slots of this stage, which stays held until every warp has
+            // read them; warp j combines chunks j and j + 4 of all four ----
+            st.reduce_l();
+            __syncwarp();
+            dump_state(st, smem + Smem::ring + (s * kTileGranules + warp) * kSlotBytes, lane);
+            named_sync(kBarStream, kStreamWarps * 32);
+            const int cs = owner_of(ustart, W, Geff);
+            const int P = owner_of(ustart + n - 1, W, Geff) - cs + 1;
+            {
+                const PieceOut po = piece_out(p, r, kvh, cs, P, cta, kFp8 ? sm_vs[kvh] : 1.f);
+                combine_dumps(po, smem + Smem::ring, nullptr, s * kTileGranules, kStreamWarps, warp,
+                              lane);
+            }
+            // Generic-proxy writes must be ordered before TMA reuses the slots.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-            if (tile == 0 && tid == 0) griddep_launch();  // as in burst mode
-            ++tile;
-            if (!(flags & kLast)) continue;
-
-            // ---- end of a piece: combine the four warps' partial softmax states ----
-            float l0 = st.l0, l1 = st.l1;
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-            }
-            if (gq == 0) {
-                sm_m[warp * 8 + 2 * tq] = st.m0;
-                sm_m[warp * 8 + 2 * tq + 1] = st.m1;
-                sm_l[warp * 8 + 2 * tq] = l0;
-                sm_l[warp * 8 + 2 * tq + 1] = l1;
-            }
-            const int uend = ustart + n;
-            const int cstart = owner_of(ustart, W, Geff);
-            const int P = owner_of(uend - 1, W, Geff) - cstart + 1;
-            const int u = r * hk + kvh;
-            const int my_slot = cta + u;  // piece slot: block + unit is unique
-            consumer_sync();
-            const int ch = tid >> 4;        // head this thread combines
-            float Mh = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, sm_m[w * 8 + ch]);
-            float wsc[kConsumerWarps];
-            float Lh = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                wsc[w] = Mh == -INFINITY ? 0.f : fast_exp2(sm_m[w * 8 + ch] - Mh);
-                Lh += wsc[w] * sm_l[w * 8 + ch];
-            }
-            float* rec = p.records + (int64_t)my_slot * p.rec_floats;
-            if (P > 1 && (tid & 15) == 0 && ch < p.group) {
-                rec[ch] = Mh;
-                rec[8 + ch] = Lh;
-            }
-            const float inv = Lh > 0.f ? __fdividef(kFp8 ? sm_vs[kvh] : 1.f, Lh) : 0.f;
-            const int cq = (tid & 15) * 4;  // four dims within a 64-dim pass
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                // warp writes its O^T fragments for dims [64 pass, 64 pass + 64)
-                float* base = sm_comb + warp * 8 * kCombStride;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int mt = 4 * pass + k;
-                    base[(2 * tq) * kCombStride + 16 * k + gq] = st.o[mt][0];
-                    base[(2 * tq + 1) * kCombStride + 16 * k + gq] = st.o[mt][1];
-                    base[(2 * tq) * kCombStride + 16 * k + gq + 8] = st.o[mt][2];
-                    base[(2 * tq + 1) * kCombStride + 16 * k + gq + 8] = st.o[mt][3];
+            if (P > 1 && tid == 0) {
+                // A contiguous range has at most two split pieces: its first and its last.
+                const int k = bp->ntasks;
+                if (k < kMaxTasks) {
+                    Task& t = bp->tasks[k];
+                    t.u = r * hk + kvh;
+                    t.cs = cs;
+                    t.P = P;
+                    t.idx = cta - cs;
+                    t.r = r;
+                    t.kvh = kvh;
+                    bp->ntasks = k + 1;
                 }
-                consumer_sync();
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float4 x =
-                        *reinterpret_cast<const float4*>(sm_comb + (w * 8 + ch) * kCombStride + cq);
-                    v.x += wsc[w] * x.x;
-                    v.y += wsc[w] * x.y;
-                    v.z += wsc[w] * x.z;
-                    v.w += wsc[w] * x.w;
-                }
-                const int dd = 64 * pass + cq;
-                if (ch < p.group) {
-                    if (P == 1) {
-                        uint2 pk;
-                        pk.x = pack_half2(v.x * inv, v.y * inv);
-                        pk.y = pack_half2(v.z * inv, v.w * inv);
-                        *reinterpret_cast<uint2*>(
-                            p.out + ((int64_t)r * p.hq + kvh * p.group + ch) * kHeadDim + dd) = pk;
-                    } else {
-                        *reinterpret_cast<float4*>(rec + kRecHead + ch * kHeadDim + dd) = v;
-                    }
-                }
-                consumer_sync();
-            }
-            if (P == 1) continue;
-            // A split piece: its record is published; its arrival is counted once
-            // per block, after the block's last piece (a contiguous range has at
-            // most two split pieces: its first and its last).
-            if (tid == 0) {
-                const int k = sm_flags[3];
-                sm_flags[4 + 5 * k] = u;
-                sm_flags[5 + 5 * k] = cstart;
-                sm_flags[6 + 5 * k] = P;
-                sm_flags[7 + 5 * k] = r;
-                sm_flags[8 + 5 * k] = kvh;
-                sm_flags[3] = k + 1;
             }
         }
+        // the ring is idle once every stage is consumed
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_sync(kBarStream, kStreamWarps * 32);
     }
 
-    // ---- split pieces.  Every piece publishes its record and counts itself
-    // on the unit's counter with a release.  The block holding the unit's
-    // last piece waits (bounded) until all P pieces have counted, lands their
-    // records and combines them through their log-sum-exp, then re-arms the
-    // counter.  A block merges at most one unit: the one whose end is its
-    // first piece.  (Splitting a long unit's merge over several blocks, one
-    // query head each, measured slower.) ----
-    // Shared memory written through the generic proxy (partials, patches) is
-    // ordered before the bulk copies that may land records over it, and the
-    // records written here before the bulk copies that may read them back.
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    consumer_sync();
-    const int nsplit = sm_flags[3];
-    if (nsplit == 0 || sm_flags[0]) return;
-    if (tid < nsplit) {
-        // The barrier above orders every thread's record stores before this
-        // thread's release.
-        const int u = sm_flags[4 + 5 * tid];
-        const int cs = sm_flags[5 + 5 * tid];
-        const int P = sm_flags[6 + 5 * tid];
-        int* ctr = p.counters + (int64_t)u * kCounterStride;
-        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
-        int merge = 0;
-        if (cta == cs + P - 1) {
-            // the acquire makes every piece's record visible to this block
-            // after the next barrier
-            int seen = 0;
-            for (uint32_t i = 0; i < kPollLimit; ++i) {
-                asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
-                if (seen >= P) break;
-                __nanosleep(32);
-            }
-            if (seen >= P) {
-                *ctr = 0;  // every piece has arrived: re-arm for the next call
-                merge = 1;
-            } else {
-                sm_flags[0] = 1;
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            }
-        }
-        sm_flags[14 + tid] = merge;
-    }
-    consumer_sync();
+    // ---- merges: the block's split pieces that make it a participant; with
+    // two tasks the consumer warps are halved between them ----
     if (sm_flags[0]) return;
-    int job = -1;
-    for (int k = 0; k < nsplit; ++k)
-        if (sm_flags[14 + k]) job = k;
-    if (job < 0) return;
-    const int u = sm_flags[4 + 5 * job], cs = sm_flags[5 + 5 * job], P = sm_flags[6 + 5 * job];
-    const int r = sm_flags[7 + 5 * job], kvh = sm_flags[8 + 5 * job];
-    const float vs = kFp8 ? sm_vs[kvh] : 1.f;
-    const uint32_t rec_bytes = (uint32_t)p.rec_floats * 4u;
-    // The ring is idle once the block's granules are consumed: the records
-    // land there by bulk copies issued at once, in batches of kMergeBatch
-    // with a barrier each, and each batch is merged as soon as it has landed.
-    // A unit with more records than the ring or the barriers take is merged
-    // from the workspace directly.
-    const bool landing =
-        P <= kLandMax && (uint32_t)P * rec_bytes <= (uint32_t)(kRing * kSlotBytes);
-    if (landing && warp == 0) {
-        // a unit's records sit in consecutive workspace slots: one copy per batch
-        const int nbat = (P + kMergeBatch - 1) / kMergeBatch;
-        if (lane < nbat) {
-            const uint32_t bytes = (uint32_t)min(kMergeBatch, P - lane * kMergeBatch) * rec_bytes;
-            mbar_arrive_expect_tx(bar_merge + 8 * lane, bytes);
-            bulk_load(sbase + Smem::ring + lane * kMergeBatch * rec_bytes,
-                      p.records + (int64_t)(cs + u + lane * kMergeBatch) * p.rec_floats, bytes,
-                      bar_merge + 8 * lane);
-        }
-    }
-    const int mh = tid >> 4;        // head
-    const int md = (tid & 15) * 4;  // dims md..md+3 and md+64..md+67
-    const bool mine = mh < p.group;
-    float M = -INFINITY, Ls = 0.f, Ls2 = 0.f, acc[8], acc2[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = acc2[i] = 0.f;
-    for (int j0 = 0; j0 < P; j0 += kMergeBatch) {
-        if (landing) {
-            if (!mbar_wait(bar_merge + 8 * (j0 / kMergeBatch), 0)) {
-                if (lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                return;
-            }
-            if (mine)
-                merge_batch<false>(reinterpret_cast<const float*>(smem + Smem::ring), j0, P,
-                                   p.rec_floats, mh, md, M, Ls, Ls2, acc, acc2);
-        } else if (mine) {
-            merge_batch<true>(p.records + (int64_t)(cs + u) * p.rec_floats, j0, P, p.rec_floats, mh,
-                              md, M, Ls, Ls2, acc, acc2);
-        }
-    }
-    if (mine) {
-        const float L = Ls + Ls2;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += acc2[i];
-        const float iv = L > 0.f ? __fdividef(vs, L) : 0.f;
-        __half* orow = p.out + ((int64_t)r * p.hq + kvh * p.group + mh) * kHeadDim;
-        *reinterpret_cast<uint2*>(orow + md) =
-            make_uint2(pack_half2(acc[0] * iv, acc[1] * iv), pack_half2(acc[2] * iv, acc[3] * iv));
-        *reinterpret_cast<uint2*>(orow + md + 64) =
-            make_uint2(pack_half2(acc[4] * iv, acc[5] * iv), pack_half2(acc[6] * iv, acc[7] * iv));
+    const int ntask = bp->ntasks;
+    if (ntask == 0) return;
+    const int nc = burst ? kConsumerWarps : kStreamWarps;
+    const int half = nc / 2;
+    const int t = ntask == 1 ? 0 : (warp < half ? 0 : 1);
+    const int lw = (ntask == 1 || warp < half) ? warp : warp - half;
+    const int nw = ntask == 1 ? nc : (t == 0 ? half : nc - half);
+    const Task task = bp->tasks[t];
+    merge_task(p, task, lw, nw, smem + Smem::ring + t * kLandBytes, kBarMerge + t,
+               kFp8 ? sm_vs[task.kvh] : 1.f, sm_flags + 4 + t, lane);
+}
+
+// The plan of a step: one block scans the lengths once, then warp w makes
+// the plans of blocks w, w + 32, ... and copies each out as 32 x 16 bytes.
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    decode_plan_kernel(const Params p, unsigned char* plan, int G) {
+    extern __shared__ __align__(16) unsigned char psm[];
+    BlockPlan* bps = reinterpret_cast<BlockPlan*>(psm);
+    int* part = reinterpret_cast<int*>(psm + (kPlanThreads / 32) * kPlanBytes);
+    int* pre = part + kPlanThreads;
+    int* len = pre + p.rows + 1;
+    const int W = scan_lengths<kPlanThreads>(p, true, pre, len, part, true);
+    const int Geff = W < G ? W : G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = warp; b < G; b += kPlanThreads / 32) {
+        build_block_plan(bps + warp, p, true, b, G, W, Geff, pre, len, lane);
+        reinterpret_cast<uint4*>(plan + (size_t)b * kPlanBytes)[lane] =
+            reinterpret_cast<const uint4*>(bps + warp)[lane];
+        __syncwarp();
     }
 }
 
@@ -1444,6 +1562,20 @@ static int device_info(DeviceInfo** out) {
     return PKV_OK;
 }
 
+// Blocks of a decode launch: one per SM, at most kMaxCtas and at most one per
+// granule the sizes allow.  The plan and the decode launch agree on it.
+static int decode_grid(int rows, int kv_heads, int limit, int* grid) {
+    DeviceInfo* info = nullptr;
+    const int st = device_info(&info);
+    if (st != PKV_OK) return st;
+    const int64_t granules = (int64_t)rows * kv_heads * ((limit + kGranule - 1) / kGranule);
+    int64_t ctas = info->sms;
+    if (ctas > kMaxCtas) ctas = kMaxCtas;
+    if (ctas > granules) ctas = granules > 0 ? granules : 1;
+    *grid = (int)ctas;
+    return PKV_OK;
+}
+
 }  // namespace tma
 
 bool tma_decode_supported(int rows, int q_heads, int kv_heads, int head_dim, int block_size) {
@@ -1452,30 +1584,59 @@ bool tma_decode_supported(int rows, int q_heads, int kv_heads, int head_dim, int
            rows <= tma::kMaxRows;
 }
 
+// Record slots a launch may use: one per block plus one per unit (a unit's
+// records start at slot first block + unit).  Blocks are one per SM of the
+// current device, so a workspace sized here serves any device with at most as
+// many SMs.
 static int64_t tma_slots(int rows, int kv_heads, int max_seq_len) {
     const int64_t units = (int64_t)rows * kv_heads;
-    const int64_t granules = units * ((max_seq_len + tma::kGranule - 1) / tma::kGranule);
-    const int64_t ctas = granules < tma::kMaxCtas ? (granules > 0 ? granules : 1) : tma::kMaxCtas;
-    return ctas + units;  // piece slot = block + unit
-}
-
-static size_t tma_counter_bytes(int rows, int kv_heads) {
-    // one counter per 128-byte line: arrivals on different units never
-    // queue on the same L2 line
-    return align_up((size_t)tma::kCounterStride * sizeof(int) * (size_t)rows * (size_t)kv_heads, 256);
+    int ctas = tma::kMaxCtas;
+    if (tma::decode_grid(rows, kv_heads, max_seq_len, &ctas) != PKV_OK) ctas = tma::kMaxCtas;
+    return ctas + units;
 }
 
 size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len) {
-    const int group = kv_heads > 0 ? q_heads / kv_heads : 0;
-    return tma_counter_bytes(rows, kv_heads) +
-           align_up(sizeof(float) * (size_t)(tma::kRecHead + group * kHeadDim) *
-                        (size_t)tma_slots(rows, kv_heads, max_seq_len),
-                    256);
+    (void)q_heads;
+    return align_up((size_t)tma::kRecBytes * (size_t)tma_slots(rows, kv_heads, max_seq_len), 256);
+}
+
+size_t tma_plan_bytes(int rows, int kv_heads, int max_seq_len) {
+    const int64_t granules = (int64_t)rows * kv_heads * ((max_seq_len + tma::kGranule - 1) / tma::kGranule);
+    const int64_t ctas = granules < tma::kMaxCtas ? (granules > 0 ? granules : 1) : tma::kMaxCtas;
+    return (size_t)ctas * tma::kPlanBytes;
+}
+
+int tma_plan_launch(void* plan, size_t plan_bytes, const int32_t* tables, const int32_t* seq_lens,
+                    const int32_t* positions, int rows, int q_heads, int kv_heads, int block_size,
+                    int mbpr, int num_blocks, int max_seq_len, int32_t* dev_err,
+                    cudaStream_t stream) {
+    using namespace tma;
+    if ((int64_t)num_blocks * block_size >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    int G = 0;
+    int st = decode_grid(rows, kv_heads, max_seq_len, &G);
+    if (st != PKV_OK) return st;
+    if (plan_bytes < (size_t)G * kPlanBytes) return PKV_ERR_WORKSPACE;
+    Params prm{};
+    prm.tables = tables;
+    prm.seq_lens = seq_lens;
+    prm.rows = rows;
+    prm.hq = q_heads;
+    prm.hk = kv_heads;
+    prm.group = q_heads / kv_heads;
+    prm.bs = block_size;
+    prm.mbpr = mbpr;
+    prm.nb = num_blocks;
+    prm.limit = max_seq_len;
+    prm.dev_err = dev_err;
+    prm.positions = positions;
+    const size_t smem = (kPlanThreads / 32) * kPlanBytes + kPlanThreads * 4 + (size_t)(2 * rows + 1) * 4;
+    decode_plan_kernel<<<1, kPlanThreads, smem, stream>>>(prm, static_cast<unsigned char*>(plan), G);
+    return launch_status();
 }
 
 size_t tma_workspace_zero_bytes(int rows, int kv_heads, int max_seq_len) {
-    (void)max_seq_len;
-    return tma_counter_bytes(rows, kv_heads);  // the per-unit arrival counters
+    // every record word starts cleared (and each call leaves them so)
+    return align_up((size_t)tma::kRecBytes * (size_t)tma_slots(rows, kv_heads, max_seq_len), 256);
 }
 
 int tma_decode_launch(void* out, const void* q, const void* k_base, const void* v_base,
@@ -1483,7 +1644,7 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
                       int max_seq_len, int width, void* workspace, int32_t* dev_err,
                       cudaStream_t stream, const AppendArgs* append, bool pdl,
-                      const float* k_scale, const float* v_scale) {
+                      const float* k_scale, const float* v_scale, const void* plan) {
     using namespace tma;
     const bool paged = width == 0;
     const bool fp8 = k_scale != nullptr;
@@ -1497,13 +1658,12 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     DeviceInfo* info = nullptr;
     int st = device_info(&info);
     if (st != PKV_OK) return st;
+    int ctas = 0;
+    if ((st = decode_grid(rows, kv_heads, limit, &ctas)) != PKV_OK) return st;
+    if (plan && !paged) return PKV_ERR_UNSUPPORTED;
     CUtensorMap km, vm;
     if ((st = pool_map(k_base, pool_rows, kv_heads, fp8, &km)) != PKV_OK) return st;
     if ((st = pool_map(v_base, pool_rows, kv_heads, fp8, &vm)) != PKV_OK) return st;
-
-    int64_t ctas = info->sms;
-    if (ctas > kMaxCtas) ctas = kMaxCtas;
-    if (ctas > granules) ctas = granules > 0 ? granules : 1;
 
     Params prm{};
     prm.out = static_cast<__half*>(out);
@@ -1520,10 +1680,9 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     prm.limit = limit;
     prm.width = paged ? 0 : width;
     prm.scale_log2 = scale * kLog2e;
-    prm.rec_floats = kRecHead + prm.group * kHeadDim;
-    prm.counters = static_cast<int*>(workspace);
-    prm.records = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                           tma_counter_bytes(rows, kv_heads));
+    prm.poll_limit = kPollLimit;
+    prm.plan = static_cast<const unsigned char*>(plan);
+    prm.records = static_cast<unsigned char*>(workspace);
     prm.dev_err = dev_err;
     if (append) {
         prm.positions = append->positions;

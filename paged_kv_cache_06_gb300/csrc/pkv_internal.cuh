@@ -45,6 +45,12 @@ size_t decode_workspace_zero_bytes(int rows, int q_heads, int kv_heads, int head
 bool tma_decode_supported(int rows, int q_heads, int kv_heads, int head_dim, int block_size);
 size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len);
 size_t tma_workspace_zero_bytes(int rows, int kv_heads, int max_seq_len);
+// Per-step decode plan (decode_tma.cu): bytes for these sizes, and its launch.
+size_t tma_plan_bytes(int rows, int kv_heads, int max_seq_len);
+int tma_plan_launch(void* plan, size_t plan_bytes, const int32_t* tables, const int32_t* seq_lens,
+                    const int32_t* positions, int rows, int q_heads, int kv_heads, int block_size,
+                    int mbpr, int num_blocks, int max_seq_len, int32_t* dev_err,
+                    cudaStream_t stream);
 // New-token append fused into the decode launch (positions / k_new / v_new as
 // in paged_kv_append).
 struct AppendArgs {
@@ -69,6 +75,7 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
                       int kv_heads, int block_size, float scale, int mbpr, int num_blocks,
                       int max_seq_len, int width, void* workspace, int32_t* dev_err,
                       cudaStream_t stream, const AppendArgs* append = nullptr, bool pdl = false,
-                      const float* k_scale = nullptr, const float* v_scale = nullptr);
+                      const float* k_scale = nullptr, const float* v_scale = nullptr,
+                      const void* plan = nullptr);
 
 }  // namespace pkv

@@ -86,6 +86,13 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_kv_copy_blocks.restype = I
     L.paged_kv_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
     L.paged_kv_prefill_scatter.restype = I
+    L.paged_attention_plan_size.argtypes = [I, I, I, I, I, I]
+    L.paged_attention_plan_size.restype = S
+    L.paged_attention_plan.argtypes = [P, S, P, P, P, I, I, I, I, I, I, I, I, P, P]
+    L.paged_attention_plan.restype = I
+    L.paged_attention_decode_planned.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F,
+                                                 I, I, I, P, S, P, S, ctypes.c_uint, P, P]
+    L.paged_attention_decode_planned.restype = I
 
 
 def status_string(status: int) -> str:
@@ -362,6 +369,72 @@ def decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale: float,
                                               bs, float(scale), block_tables.shape[1], nb,
                                               int(max_seq_len), _ptr(dev_err), _stream(stream))
     _check("paged_attention_decode_noalloc", st)
+
+
+def plan_size(rows: int, q_heads: int, kv_heads: int, head_dim: int, max_seq_len: int,
+              block_size: int) -> int:
+    return int(lib().paged_attention_plan_size(rows, q_heads, kv_heads, head_dim, max_seq_len,
+                                               block_size))
+
+
+def alloc_plan(rows, q_heads, kv_heads, head_dim, max_seq_len, block_size, device="cuda"):
+    """A plan buffer of the size the C ABI asks for."""
+    n = plan_size(rows, q_heads, kv_heads, head_dim, max_seq_len, block_size)
+    if n == 0:
+        raise ValueError("unsupported sizes for paged_attention_plan")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def plan(plan_buf, block_tables, seq_lens, positions, q_heads: int, kv_heads: int, head_dim: int,
+         block_size: int, num_blocks: int, max_seq_len: int, dev_err=None, stream=None):
+    """paged_attention_plan: the work split of one decode step, shared by its
+    layers (``positions`` may be None when the step appends nothing)."""
+    for t, n, dt, nd in ((plan_buf, "plan", torch.uint8, 1),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1)):
+        _need(t, n, dt, nd)
+    if positions is not None:
+        _need(positions, "positions", torch.int32, 1)
+    _need_err(dev_err)
+    rows = seq_lens.shape[0]
+    st = lib().paged_attention_plan(_ptr(plan_buf), plan_buf.numel(), _ptr(block_tables),
+                                    _ptr(seq_lens), _ptr(positions), rows, q_heads, kv_heads,
+                                    head_dim, block_size, block_tables.shape[1], num_blocks,
+                                    int(max_seq_len), _ptr(dev_err), _stream(stream))
+    _check("paged_attention_plan", st)
+
+
+def decode_planned(out, q, k_pool, v_pool, block_tables, seq_lens, scale: float, max_seq_len: int,
+                   plan_buf, workspace, positions=None, k_new=None, v_new=None, k_scale=None,
+                   v_scale=None, pdl: bool = False, dev_err=None, stream=None):
+    """paged_attention_decode_planned: one layer of a planned step (append +
+    decode when ``positions`` is given; FP8 pools when the scales are)."""
+    fp8 = k_scale is not None
+    pool_dt = torch.uint8 if fp8 else torch.float16
+    for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
+                         (k_pool, "k_pool", pool_dt, 4), (v_pool, "v_pool", pool_dt, 4),
+                         (block_tables, "block_tables", torch.int32, 2),
+                         (seq_lens, "seq_lens", torch.int32, 1),
+                         (plan_buf, "plan", torch.uint8, 1),
+                         (workspace, "workspace", torch.uint8, 1)):
+        _need(t, n, dt, nd)
+    if fp8:
+        _need(k_scale, "k_scale", torch.float32, 1)
+        _need(v_scale, "v_scale", torch.float32, 1)
+    if positions is not None:
+        _need(positions, "positions", torch.int32, 1)
+        _need(k_new, "k_new", torch.float16, 3)
+        _need(v_new, "v_new", torch.float16, 3)
+    _need_err(dev_err)
+    rows, hq, d = q.shape
+    nb, bs, hk, _ = k_pool.shape
+    st = lib().paged_attention_decode_planned(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(seq_lens), _ptr(positions), _ptr(k_new), _ptr(v_new), rows, hq,
+        hk, d, bs, float(scale), block_tables.shape[1], nb, int(max_seq_len), _ptr(plan_buf),
+        plan_buf.numel(), _ptr(workspace), workspace.numel(), PKV_FLAG_PDL if pdl else 0,
+        _ptr(dev_err), _stream(stream))
+    _check("paged_attention_decode_planned", st)
 
 
 def check_error(dev_err: torch.Tensor, stream=None) -> int:
