@@ -1492,14 +1492,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_sync(kBarStream, kStreamWarps * 32);
     }
 
-    // ---- merges: the block's split pieces that make it a participant; with
-    // two tasks the consumer warps are halved between them ----
+    // ---- merges: the block's split pieces that make it a participant (the
+    // first min(P, 8) pieces of their unit); with two such tasks the
+    // consumer warps are halved between them ----
     if (sm_flags[0]) return;
-    const int ntask = bp->ntasks;
+    int ntask = 0, first = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxTasks; ++k) {
+        if (k >= bp->ntasks) break;
+        const Task& tk = bp->tasks[k];
+        if (tk.idx < (tk.P < kMergeWays ? tk.P : kMergeWays)) {
+            if (ntask == 0) first = k;
+            ++ntask;
+        }
+    }
     if (ntask == 0) return;
     const int nc = burst ? kConsumerWarps : kStreamWarps;
     const int half = nc / 2;
-    const int t = ntask == 1 ? 0 : (warp < half ? 0 : 1);
+    const int t = ntask == 1 ? first : (warp < half ? 0 : 1);
     const int lw = (ntask == 1 || warp < half) ? warp : warp - half;
     const int nw = ntask == 1 ? nc : (t == 0 ? half : nc - half);
     const Task task = bp->tasks[t];
