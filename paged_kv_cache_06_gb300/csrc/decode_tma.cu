@@ -425,9 +425,10 @@ __device__ __forceinline__ void store_chunk(__half* ob, int c, const float (&o)[
 // words it took, so the workspace is all zero between calls.
 //
 // Region of unit u (pieces in blocks cs .. cs+P-1) at slot cs + u: chunk c of
-// piece i at ((c*P + i)*32 + lane) * 32 bytes (the lane's four floats), then
-// m/l of piece i for participant k at 8*P*1 KB + (k*P + i)*128 + tq*32
-// (m[2tq], m[2tq+1], l[2tq], l[2tq+1]).  Participant k reads chunks
+// piece i at (c*P + i) KB, the lanes' first two floats at 16*lane and their
+// last two at 512 + 16*lane (so a warp's stores fill whole sectors), then m/l
+// of piece i for participant k at 8*P KB + (k*P + i)*128: m[2tq], m[2tq+1] at
+// 16*tq and l[2tq], l[2tq+1] at 64 + 16*tq.  Participant k reads chunks
 // c = k, k + K, ... of every piece and its own m/l copies, so no word is
 // read by two blocks.
 constexpr uint32_t kLLChunk = 32 * 4 * 8;   // one chunk of a state as words: 1 KB
@@ -480,9 +481,9 @@ __device__ __forceinline__ void emit_chunk(const PieceOut& po, int c, const floa
         const float inv1 = L1 > 0.f ? __fdividef(po.vs, L1) : 0.f;
         store_chunk(po.ob, c, acc, inv0, inv1, po.group, lane);
     } else {
-        unsigned char* a = po.region + (size_t)(c * po.P + po.idx) * kLLChunk + lane * 32;
+        unsigned char* a = po.region + (size_t)(c * po.P + po.idx) * kLLChunk + lane * 16;
         st_words(a, acc[0], acc[1]);
-        st_words(a + 16, acc[2], acc[3]);
+        st_words(a + 512, acc[2], acc[3]);
     }
 }
 // m/l of a split piece, one copy per participant (lanes 0-3).
@@ -492,9 +493,9 @@ __device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, 
 #pragma unroll 1
     for (int k = 0; k < po.K; ++k) {
         unsigned char* a =
-            po.region + (size_t)8 * po.P * kLLChunk + (size_t)(k * po.P + po.idx) * kLLMl + lane * 32;
+            po.region + (size_t)8 * po.P * kLLChunk + (size_t)(k * po.P + po.idx) * kLLMl + lane * 16;
         st_words(a, M0, M1);
-        st_words(a + 16, L0, L1);
+        st_words(a + 64, L0, L1);
     }
 }
 
@@ -507,12 +508,12 @@ __device__ __forceinline__ void finish_own(const PieceOut& po, const Soft& st, i
         for (int c = 0; c < 8; ++c) store_chunk(po.ob, c, st.o[c], inv0, inv1, po.group, lane);
         return;
     }
-    unsigned char* a = po.region + (size_t)po.idx * kLLChunk + lane * 32;
+    unsigned char* a = po.region + (size_t)po.idx * kLLChunk + lane * 16;
     const size_t step = (size_t)po.P * kLLChunk;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         st_words(a + c * step, st.o[c][0], st.o[c][1]);
-        st_words(a + c * step + 16, st.o[c][2], st.o[c][3]);
+        st_words(a + c * step + 512, st.o[c][2], st.o[c][3]);
     }
     emit_ml(po, st.m0, st.m1, st.l0, st.l1, lane);
 }
@@ -590,14 +591,14 @@ __device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsig
     const bool active = q < gsz;
     const int tq = lane & 3;
     unsigned char* reg = unit_region(p, t.u, t.cs);
-    unsigned char* mlb = reg + (size_t)8 * P * kLLChunk + (size_t)t.idx * P * kLLMl + tq * 32;
+    unsigned char* mlb = reg + (size_t)8 * P * kLLChunk + (size_t)t.idx * P * kLLMl + tq * 16;
     __half* ob = p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim;
     bool ok = true;
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int m = g; active && m < nch; m += groups) {
         const int c = t.idx + m * K;
-        const unsigned char* cb = reg + (size_t)c * P * kLLChunk + lane * 32;
+        const unsigned char* cb = reg + (size_t)c * P * kLLChunk + lane * 16;
         M0 = M1 = -INFINITY;
         L0 = L1 = 0.f;
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -613,9 +614,9 @@ __device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsig
                     const int j = j0 + b * gsz;
                     if (j >= P) continue;
                     ld_words(mlb + j * kLLMl, w[b][0], w[b][1]);
-                    ld_words(mlb + j * kLLMl + 16, w[b][2], w[b][3]);
+                    ld_words(mlb + j * kLLMl + 64, w[b][2], w[b][3]);
                     ld_words(cb + j * kLLChunk, w[b][4], w[b][5]);
-                    ld_words(cb + j * kLLChunk + 16, w[b][6], w[b][7]);
+                    ld_words(cb + j * kLLChunk + 512, w[b][6], w[b][7]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) all &= flagged(w[b][e]);
                 }
@@ -662,7 +663,7 @@ __device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsig
                 // taken: clear the chunk words (read by this warp alone) for the
                 // next call; the m/l words are shared by the task's warps
                 clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk);
-                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk + 16);
+                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk + 512);
             }
         }
         if (gsz == 1 && ok) {
@@ -687,7 +688,7 @@ __device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsig
 #pragma unroll 1
     for (int j = lw; j < P; j += nw) {
         clear_words(mlb + j * kLLMl);
-        clear_words(mlb + j * kLLMl + 16);
+        clear_words(mlb + j * kLLMl + 64);
     }
     if (gsz == 1 || q != 0) return true;
     // the group's partials (at most kConsumerWarps), all loaded up front
