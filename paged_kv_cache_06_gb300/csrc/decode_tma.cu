@@ -19,18 +19,23 @@
 // all the layers of the step.  The part of a unit inside one block is a
 // piece.
 //
-// Block layout.  Warp 7 is the producer: it resolves each granule's physical
-// block from the table and issues TMA tiled copies (a 16-token x 64-dim box,
-// 128-byte swizzle, never crossing a physical block) into a ring of twelve
-// 8 KB granule slots.  Warps 0-6 consume, in one of two modes:
-//   * burst: the block's whole range fits the ring and covers at most four
-//     pieces.  Every copy is issued before the dependency wait, the seven
-//     warps are dealt to pieces in proportion to their size, and each warp
-//     attends to its granules; each piece's first warp then absorbs the
-//     states of the piece's other warps.
-//   * stream: the ring runs as three stages of four granules, one granule
-//     per warp (warps 0-3) per stage, and warp 0 absorbs the others' states
-//     as each piece ends.
+// Block layout.  Warps 0-6 consume, warp 7 produces, in one of two modes:
+//   * burst: the block's whole range fits the ring of twelve 8 KB granule
+//     slots and covers at most four pieces.  The seven consumer warps are
+//     dealt to pieces in proportion to their size; before the dependency
+//     wait each stages its own granules with 16-byte cp.async copies (rows
+//     past the length zero-filled), each then attends to its granules, and
+//     the warps of a piece combine their states.  Warp 7 only does the
+//     block's row work (the fused append).  Plain asynchronous copies are
+//     used here because, in a grid launched with programmatic stream
+//     serialization, tiled bulk copies issued before the dependency wait
+//     complete only after the preceding grid has completed, while plain
+//     loads and cp.async proceed at once.
+//   * stream: the producer resolves each granule's physical block from the
+//     table and issues TMA tiled copies (a 16-token x 64-dim box, 128-byte
+//     swizzle, never crossing a physical block) into the ring as three
+//     stages of four granules, one granule per warp (warps 0-3) per stage,
+//     and warp 0 absorbs the others' states as each piece ends.
 // Per granule (16 tokens) and group of query heads (up to 8):
 //   S^T[16 tok][8 heads] = K[16 tok][128] . Q^T        (mma.sync m16n8k16)
 //   online softmax per head in fp32, base-2 exponent
@@ -50,11 +55,11 @@
 // merging the chunks c with c % K == k.  Every piece writes its combined
 // state as a record into the unit's region of the workspace (chunk-major
 // over the unit's pieces, so a participant's slice of all P records is
-// contiguous) and counts itself, with a release, on each participant's own
-// arrival counter.  A participant waits (bounded) until its counter reaches
-// P, re-arms it, lands its slice of the P records in the idle ring with one
-// bulk copy per chunk and merges them through their log-sum-exp in piece
-// order, so the result never depends on timing.
+// contiguous), each float stored as the complement of its bits so that a
+// zero word means "not yet written".  A participant polls (bounded) its
+// slice of the P records, merges them through their log-sum-exp in piece
+// order, so the result never depends on timing, and clears the words it
+// read.
 //
 // Safety: table entries are range-checked before any copy is issued (a bad
 // entry is skipped and flagged); every mbarrier wait and counter poll is
@@ -128,10 +133,15 @@ struct Params {
     const __half* v_new;
     __half* kpool;
     __half* vpool;
+    // pools (or padded slabs) as the consumers' plain copies read them
+    const void* kbase;
+    const void* vbase;
     // FP8 pools: one scale per KV head (null for fp16 pools)
     const float* k_scale;
     const float* v_scale;
 };
+
+static_assert(sizeof(Params) <= 256 && sizeof(Params) % 8 == 0, "Params fit their shared-memory copy");
 
 // A split piece of this block: its unit, the unit's first block and piece
 // count, this piece's index among them, and the unit's row and head.
@@ -170,7 +180,8 @@ struct Smem {
     static constexpr uint32_t flags = plan + kPlanBytes;                            // misc ints
     static constexpr uint32_t scales = flags + 16 * 4;                              // FP8: k, v scale [2][16]
     static constexpr uint32_t ppos = scales + 2 * kFp8MaxKvHeads * 4;               // piece positions [32]
-    static constexpr uint32_t part = ppos + kMaxPieces * 4;                         // scan partials [kThreads]
+    static constexpr uint32_t prm = ppos + kMaxPieces * 4;                          // copy of the launch's Params
+    static constexpr uint32_t part = prm + 256;                                     // scan partials [kThreads]
     static constexpr uint32_t prefix = part + kThreads * 4;                         // rows + 1 ints
     __host__ __device__ static constexpr uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
     __host__ __device__ static constexpr uint32_t total(int rows) { return lens(rows) + (uint32_t)rows * 4 + 1024; }
@@ -178,6 +189,8 @@ struct Smem {
 // Two blocks per SM (this layer's and the next one's, under programmatic
 // dependent launch) at batch 32: 228 KB per SM, 1 KB reserved per block.
 static_assert(Smem::total(32) + 1024 <= 233472 / 2, "two blocks per SM at 32 rows");
+
+__device__ __forceinline__ const void* kmap_base(const Params& p, bool v) { return v ? p.vbase : p.kbase; }
 
 // ---------------------------------------------------------------------------
 // PTX wrappers (shared ones in ptx.cuh)
@@ -320,6 +333,18 @@ __device__ __forceinline__ void load_q(uint32_t (&qb)[16], const uint32_t* qrow,
         qb[2 * ks + 1] = live ? qrow[ks * 8 + 4 + tq] : 0u;
     }
 }
+// The same from global memory, for a group's first head row `q0`: heads past
+// the group repeat its last head (every head is its own MMA column, so those
+// columns are computed and never stored).
+__device__ __forceinline__ void load_q_global(uint32_t (&qb)[16], const __half* q0, int group, int lane) {
+    const int h = (lane >> 2) < group ? (lane >> 2) : group - 1;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q0 + h * kHeadDim) + (lane & 3);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        qb[2 * ks] = qrow[ks * 8];
+        qb[2 * ks + 1] = qrow[ks * 8 + 4];
+    }
+}
 
 // Prepares a staged granule for attend: zeroes V rows past `valid` (they may
 // hold anything, NaN included) and overwrites row patch_row with the new
@@ -345,6 +370,35 @@ __device__ __forceinline__ bool prepare_granule(unsigned char* slot_ptr, int val
         wrote = true;
     }
     return wrote;
+}
+
+// Stages one granule into `slot` (shared address) with 16-byte cp.async
+// copies by one warp, in the layout the tiled copies produce: fp16 pools as
+// four boxes (K dims 0-63, K 64-127, V 0-63, V 64-127) of 16 rows x 128 B,
+// FP8 pools as a K box and a V box of 16 rows x 128 B; chunk c of row r at
+// r*128 + ((c ^ (r & 7)) << 4) (128-byte swizzle).  Rows at or past `valid`
+// are zero-filled without reading the pool.  Plain asynchronous copies are
+// used, not tiled bulk copies, because they run before the dependency wait
+// of a programmatically launched grid: bulk copies issued there complete
+// only once the preceding grid has completed.
+template <bool kFp8>
+__device__ __forceinline__ void stage_granule(uint32_t slot, const unsigned char* kpool,
+                                              const unsigned char* vpool, int64_t zrow, int hk,
+                                              int kvh, int valid, int lane) {
+    constexpr int kRowBytes = kFp8 ? 128 : 256;  // one token of one KV head
+    const int64_t row0 = (zrow * hk + kvh) * kRowBytes;
+    const uint32_t rstride = (uint32_t)hk * kRowBytes;
+    const int c = lane & 7, r0 = lane >> 3;  // chunk; first of the rows r0, r0 + 4, ...
+#pragma unroll
+    for (int k = 0; k < (kFp8 ? 8 : 16); ++k) {
+        const int r = r0 + 4 * (k & 3), b = k >> 2;  // row, box
+        const unsigned char* src = ((kFp8 ? b : b >> 1) ? vpool : kpool) + row0 +
+                                   (r < valid ? r : 0) * rstride + (kFp8 ? 0 : (b & 1) * 128) + c * 16;
+        const uint32_t dst = slot + b * kBoxBytes + r * 128 + ((c ^ (r & 7)) << 4);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                     "r"(r < valid ? 16 : 0)
+                     : "memory");
+    }
 }
 
 // FP8 pools: the producer lands a granule's E4M3 K box (16 tokens x 128
@@ -417,39 +471,48 @@ __device__ __forceinline__ void store_chunk(__half* ob, int c, const float (&o)[
 }
 
 // ---------------------------------------------------------------------------
-// Split-unit records.  Every word of a record is 8 bytes: a float's bits in
-// the low half and a flag (1) in the high half.  Naturally aligned 8-byte
-// relaxed accesses are single-copy atomic, so a reader that sees the flag
-// sees the value with it: the writer needs no fence or release and the
-// reader no separate arrival counter or second read.  The reader clears the
-// words it took, so the workspace is all zero between calls.
+// Split-unit records.  Every float of a record is stored as the bitwise
+// complement of its bits in a 4-byte word, so a zero word means "not written
+// yet": the only value that would encode as zero is the all-ones NaN pattern,
+// which the GPU's arithmetic never produces (its NaN results are canonical).
+// Naturally aligned 4-byte relaxed accesses are single-copy atomic, element
+// by element of a vector access, so a reader that sees a word non-zero sees
+// its value: the writer needs no fence or release and the reader no separate
+// arrival counter or second read.  The reader clears the words it took, so
+// the workspace is all zero between calls.
 //
 // Region of unit u (pieces in blocks cs .. cs+P-1) at slot cs + u: chunk c of
-// piece i at (c*P + i) KB, the lanes' first two floats at 16*lane and their
-// last two at 512 + 16*lane (so a warp's stores fill whole sectors), then m/l
-// of piece i for participant k at 8*P KB + (k*P + i)*128: m[2tq], m[2tq+1] at
-// 16*tq and l[2tq], l[2tq+1] at 64 + 16*tq.  Participant k reads chunks
-// c = k, k + K, ... of every piece and its own m/l copies, so no word is
-// read by two blocks.
-constexpr uint32_t kLLChunk = 32 * 4 * 8;   // one chunk of a state as words: 1 KB
-constexpr uint32_t kLLMl = 4 * 4 * 8;       // m/l of one piece for one participant
+// piece i at (c*P + i) * 512 B, lane-major (16 bytes per lane: a warp's store
+// fills whole sectors), then m/l of piece i for participant k at 8*P*512 +
+// (k*P + i)*64: m[2tq], m[2tq+1], l[2tq], l[2tq+1] at 16*tq.  Participant k
+// reads chunks c = k, k + K, ... of every piece and its own m/l copies, so no
+// word is read by two blocks.
+constexpr uint32_t kLLChunk = 32 * 16;      // one chunk of a state: 512 B
+constexpr uint32_t kLLMl = 4 * 16;          // m/l of one piece for one participant
 constexpr uint32_t kRecBytes = 8 * kLLChunk + kMergeWays * kLLMl;  // per record slot
 
 __device__ __forceinline__ unsigned char* unit_region(const Params& p, int u, int cs) {
     return p.records + (int64_t)(cs + u) * kRecBytes;
 }
-__device__ __forceinline__ void st_words(unsigned char* a, float x, float y) {
-    const uint64_t w0 = (1ull << 32) | __float_as_uint(x), w1 = (1ull << 32) | __float_as_uint(y);
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(a), "l"(w0), "l"(w1) : "memory");
+__device__ __forceinline__ void st_rec(unsigned char* a, float x, float y, float z, float w) {
+    asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(a),
+                 "r"(~__float_as_uint(x)), "r"(~__float_as_uint(y)), "r"(~__float_as_uint(z)),
+                 "r"(~__float_as_uint(w))
+                 : "memory");
 }
-__device__ __forceinline__ void clear_words(unsigned char* a) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %1};" ::"l"(a), "l"(0ull) : "memory");
+__device__ __forceinline__ void clear_rec(unsigned char* a) {
+    asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %1, %1, %1};" ::"l"(a), "r"(0u) : "memory");
 }
-__device__ __forceinline__ void ld_words(const unsigned char* a, uint64_t& w0, uint64_t& w1) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(a) : "memory");
+__device__ __forceinline__ uint4 ld_rec(const unsigned char* a) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(a)
+                 : "memory");
+    return v;
 }
-__device__ __forceinline__ bool flagged(uint64_t w) { return (w >> 32) == 1u; }
-__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ bool rec_written(const uint4& v) { return v.x && v.y && v.z && v.w; }
+__device__ __forceinline__ float rec_value(uint32_t w) { return __uint_as_float(~w); }
 
 // Where a piece's combined state goes: its unit's fp16 output rows (P == 1),
 // or its record (P > 1, piece idx of the unit, K participants).
@@ -481,9 +544,8 @@ __device__ __forceinline__ void emit_chunk(const PieceOut& po, int c, const floa
         const float inv1 = L1 > 0.f ? __fdividef(po.vs, L1) : 0.f;
         store_chunk(po.ob, c, acc, inv0, inv1, po.group, lane);
     } else {
-        unsigned char* a = po.region + (size_t)(c * po.P + po.idx) * kLLChunk + lane * 16;
-        st_words(a, acc[0], acc[1]);
-        st_words(a + 512, acc[2], acc[3]);
+        st_rec(po.region + (uint32_t)(c * po.P + po.idx) * kLLChunk + lane * 16, acc[0], acc[1], acc[2],
+               acc[3]);
     }
 }
 // m/l of a split piece, one copy per participant (lanes 0-3).
@@ -491,31 +553,9 @@ __device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, 
                                         int lane) {
     if (po.P == 1 || lane >= 4) return;
 #pragma unroll 1
-    for (int k = 0; k < po.K; ++k) {
-        unsigned char* a =
-            po.region + (size_t)8 * po.P * kLLChunk + (size_t)(k * po.P + po.idx) * kLLMl + lane * 16;
-        st_words(a, M0, M1);
-        st_words(a + 64, L0, L1);
-    }
-}
-
-// A piece held by one warp (l reduced): emits every chunk and the m/l.
-__device__ __forceinline__ void finish_own(const PieceOut& po, const Soft& st, int lane) {
-    if (po.P == 1) {
-        const float inv0 = st.l0 > 0.f ? __fdividef(po.vs, st.l0) : 0.f;
-        const float inv1 = st.l1 > 0.f ? __fdividef(po.vs, st.l1) : 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) store_chunk(po.ob, c, st.o[c], inv0, inv1, po.group, lane);
-        return;
-    }
-    unsigned char* a = po.region + (size_t)po.idx * kLLChunk + lane * 16;
-    const size_t step = (size_t)po.P * kLLChunk;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        st_words(a + c * step, st.o[c][0], st.o[c][1]);
-        st_words(a + c * step + 512, st.o[c][2], st.o[c][3]);
-    }
-    emit_ml(po, st.m0, st.m1, st.l0, st.l1, lane);
+    for (int k = 0; k < po.K; ++k)
+        st_rec(po.region + 8u * po.P * kLLChunk + (uint32_t)(k * po.P + po.idx) * kLLMl + lane * 16, M0,
+               M1, L0, L1);
 }
 
 // Warp j of a piece's k warps (k <= kConsumerWarps), whose states are dumped
@@ -550,7 +590,6 @@ __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring, con
         L0 += ml[s].x * ml[s].z;
         L1 += ml[s].y * ml[s].w;
     }
-#pragma unroll 1
     for (int c = j; c < 8; c += k) {
         float4 v[kConsumerWarps];
 #pragma unroll
@@ -574,111 +613,95 @@ __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring, con
 // c_m = idx + m*K for m < nch.  The task's nw warps form min(nch, nw) chunk
 // groups of gsz = nw / groups warps; the warp of rank q in group g merges
 // chunks m = g, g + groups, ... over records j = q, q + gsz, ..., polled in
-// batches of four, each batch taken once all its words are flagged, absorbed
-// in order (online maximum) and cleared.  With gsz > 1 the group's partials
-// meet in shared memory at `part` after the task's barrier and rank 0
-// combines them in rank order; the result never depends on timing.
-// Returns false if a poll gave up.
-__device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsigned char* part,
-                           int bar_id, float vs, volatile int* fail, int lane) {
+// batches of four, each batch taken once all its words are written, absorbed
+// in order (running maximum) and cleared.  Every warp leaves its partial of
+// each chunk in shared memory at `part`; after the task's barrier the rank-0
+// warp of each group combines its group's partials in rank order and stores
+// the chunk, so the result never depends on timing.  Returns false if a poll
+// gave up.
+__device__ __forceinline__ void absorb(float& M0, float& M1, float& L0, float& L1, float (&acc)[4],
+                                       float m0, float m1, float l0, float l1, float x0, float x1,
+                                       float x2, float x3) {
+    const float N0 = fmaxf(M0, m0), N1 = fmaxf(M1, m1);
+    const float a0 = N0 == -INFINITY ? 0.f : fast_exp2(M0 - N0);
+    const float a1 = N1 == -INFINITY ? 0.f : fast_exp2(M1 - N1);
+    const float w0 = N0 == -INFINITY ? 0.f : fast_exp2(m0 - N0);
+    const float w1 = N1 == -INFINITY ? 0.f : fast_exp2(m1 - N1);
+    L0 = L0 * a0 + w0 * l0;
+    L1 = L1 * a1 + w1 * l1;
+    acc[0] = acc[0] * a0 + w0 * x0;
+    acc[1] = acc[1] * a1 + w1 * x1;
+    acc[2] = acc[2] * a0 + w0 * x2;
+    acc[3] = acc[3] * a1 + w1 * x3;
+    M0 = N0;
+    M1 = N1;
+}
+
+__device__ __forceinline__ bool merge_task(const Params& p, const Task& t, int lw, int nw,
+                                           unsigned char* part, int bar_id, float vs,
+                                           volatile int* fail, int lane) {
     const int P = t.P;
     const int K = P < kMergeWays ? P : kMergeWays;
     if (t.idx >= K) return true;  // not a participant
-    const int nch = (kMergeWays - t.idx + K - 1) / K;
+    int nch = 0;  // chunks idx, idx + K, ... below 8
+    for (int c = t.idx; c < 8; c += K) ++nch;
     const int groups = nch < nw ? nch : nw;
-    const int gsz = nw / groups;
-    const int g = lw % groups, q = lw / groups;
-    const bool active = q < gsz;
+    int gsz = 0, g = lw, q = 0;  // nw / groups, lw % groups, lw / groups
+    for (int x = groups; x <= nw; x += groups) ++gsz;
+    while (g >= groups) {
+        g -= groups;
+        ++q;
+    }
     const int tq = lane & 3;
     unsigned char* reg = unit_region(p, t.u, t.cs);
-    unsigned char* mlb = reg + (size_t)8 * P * kLLChunk + (size_t)t.idx * P * kLLMl + tq * 16;
-    __half* ob = p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim;
+    unsigned char* mlb = reg + 8u * P * kLLChunk + (uint32_t)t.idx * P * kLLMl + tq * 16;
     bool ok = true;
-    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-    for (int m = g; active && m < nch; m += groups) {
-        const int c = t.idx + m * K;
-        const unsigned char* cb = reg + (size_t)c * P * kLLChunk + lane * 16;
-        M0 = M1 = -INFINITY;
-        L0 = L1 = 0.f;
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    for (int m = g; q < gsz && m < nch && ok; m += groups) {
+        unsigned char* cb = reg + (uint32_t)(t.idx + m * K) * P * kLLChunk + lane * 16;
+        float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (int j0 = q; j0 < P && ok; j0 += 4 * gsz) {
-            uint64_t w[4][8];
-            bool got = false;
-#pragma unroll 1
-            for (uint32_t it = 0; it < p.poll_limit; ++it) {
-                bool all = true;
+        for (int j0 = q; j0 < P; j0 += 4 * gsz) {
+            uint4 wm[4], wc[4];
+            uint32_t it = 0;
+            bool all;
+            do {
+                all = true;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const int j = j0 + b * gsz;
-                    if (j >= P) continue;
-                    ld_words(mlb + j * kLLMl, w[b][0], w[b][1]);
-                    ld_words(mlb + j * kLLMl + 64, w[b][2], w[b][3]);
-                    ld_words(cb + j * kLLChunk, w[b][4], w[b][5]);
-                    ld_words(cb + j * kLLChunk + 512, w[b][6], w[b][7]);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) all &= flagged(w[b][e]);
+                    const int j = j0 + b * gsz < P ? j0 + b * gsz : j0;  // past P: record j0 again
+                    wm[b] = ld_rec(mlb + j * kLLMl);
+                    wc[b] = ld_rec(cb + j * kLLChunk);
+                    all &= rec_written(wm[b]) & rec_written(wc[b]);
                 }
-                if (__all_sync(0xffffffffu, all)) {
-                    got = true;
-                    break;
-                }
-            }
-            if (!got) {
+            } while (!__all_sync(0xffffffffu, all) && ++it < p.poll_limit);
+            if (it >= p.poll_limit) {
                 ok = false;
                 break;
             }
-            // the batch's maximum first, then one rescale of the running sums
-            // and independent weighted adds (records past P weigh nothing)
-            float N0 = M0, N1 = M1;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                if (j0 + b * gsz >= P) continue;
-                N0 = fmaxf(N0, word_value(w[b][0]));
-                N1 = fmaxf(N1, word_value(w[b][1]));
-            }
-            const float a0 = N0 == -INFINITY ? 0.f : fast_exp2(M0 - N0);
-            const float a1 = N1 == -INFINITY ? 0.f : fast_exp2(M1 - N1);
-            L0 *= a0;
-            L1 *= a1;
-            acc[0] *= a0;
-            acc[1] *= a1;
-            acc[2] *= a0;
-            acc[3] *= a1;
-            M0 = N0;
-            M1 = N1;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int j = j0 + b * gsz;
-                if (j >= P) continue;
-                const float b0 = N0 == -INFINITY ? 0.f : fast_exp2(word_value(w[b][0]) - N0);
-                const float b1 = N1 == -INFINITY ? 0.f : fast_exp2(word_value(w[b][1]) - N1);
-                L0 += word_value(w[b][2]) * b0;
-                L1 += word_value(w[b][3]) * b1;
-                acc[0] += word_value(w[b][4]) * b0;
-                acc[1] += word_value(w[b][5]) * b1;
-                acc[2] += word_value(w[b][6]) * b0;
-                acc[3] += word_value(w[b][7]) * b1;
+                if (j >= P) break;
+                absorb(M0, M1, L0, L1, acc, rec_value(wm[b].x), rec_value(wm[b].y), rec_value(wm[b].z),
+                       rec_value(wm[b].w), rec_value(wc[b].x), rec_value(wc[b].y), rec_value(wc[b].z),
+                       rec_value(wc[b].w));
                 // taken: clear the chunk words (read by this warp alone) for the
                 // next call; the m/l words are shared by the task's warps
-                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk);
-                clear_words(const_cast<unsigned char*>(cb) + j * kLLChunk + 512);
+                clear_rec(cb + j * kLLChunk);
             }
         }
-        if (gsz == 1 && ok) {
+        if (gsz == 1) {
             const float inv0 = L0 > 0.f ? __fdividef(vs, L0) : 0.f;
             const float inv1 = L1 > 0.f ? __fdividef(vs, L1) : 0.f;
-            store_chunk(ob, c, acc, inv0, inv1, p.group, lane);
+            store_chunk(p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim, t.idx + m * K, acc, inv0, inv1, p.group, lane);
+        } else {
+            unsigned char* pw = part + (q * nch + m) * 1024 + lane * 16;
+            *reinterpret_cast<float4*>(pw) = make_float4(M0, M1, L0, L1);
+            *reinterpret_cast<float4*>(pw + 512) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
     }
     if (!ok && lane == 0) *fail = 1;
-    if (gsz > 1) {
-        // groups == nch here: each warp holds one chunk's partial
-        *reinterpret_cast<float4*>(part + lw * 1024 + lane * 16) = make_float4(M0, M1, L0, L1);
-        *reinterpret_cast<float4*>(part + lw * 1024 + 512 + lane * 16) =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
     named_sync(bar_id, nw * 32);
     if (*fail) {
         if (lane == 0 && lw == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
@@ -686,40 +709,24 @@ __device__ bool merge_task(const Params& p, const Task& t, int lw, int nw, unsig
     }
     // every warp of the task is past the m/l words: clear them for the next call
 #pragma unroll 1
-    for (int j = lw; j < P; j += nw) {
-        clear_words(mlb + j * kLLMl);
-        clear_words(mlb + j * kLLMl + 64);
+    for (int j = lw; j < P; j += nw) clear_rec(mlb + j * kLLMl);
+    if (q != 0 || gsz == 1) return true;
+    __half* ob = p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim;
+#pragma unroll 1
+    for (int m = g; m < nch; m += groups) {
+        // the group's partials of chunk m, in rank order
+        float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int r = 0; r < gsz; ++r) {
+            const unsigned char* pw = part + (r * nch + m) * 1024 + lane * 16;
+            const float4 pm = *reinterpret_cast<const float4*>(pw);
+            const float4 pv = *reinterpret_cast<const float4*>(pw + 512);
+            absorb(M0, M1, L0, L1, acc, pm.x, pm.y, pm.z, pm.w, pv.x, pv.y, pv.z, pv.w);
+        }
+        const float inv0 = L0 > 0.f ? __fdividef(vs, L0) : 0.f;
+        const float inv1 = L1 > 0.f ? __fdividef(vs, L1) : 0.f;
+        store_chunk(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
     }
-    if (gsz == 1 || q != 0) return true;
-    // the group's partials (at most kConsumerWarps), all loaded up front
-    float4 pm[kConsumerWarps], pv[kConsumerWarps];
-#pragma unroll
-    for (int r = 0; r < kConsumerWarps; ++r) {
-        const unsigned char* pw = part + (r * groups + g) * 1024 + lane * 16;
-        pm[r] = r < gsz ? *reinterpret_cast<const float4*>(pw) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
-        pv[r] = r < gsz ? *reinterpret_cast<const float4*>(pw + 512) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float G0 = -INFINITY, G1 = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kConsumerWarps; ++r) {
-        G0 = fmaxf(G0, pm[r].x);
-        G1 = fmaxf(G1, pm[r].y);
-    }
-    float S0 = 0.f, S1 = 0.f, out4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < kConsumerWarps; ++r) {
-        const float w0 = G0 == -INFINITY ? 0.f : fast_exp2(pm[r].x - G0);
-        const float w1 = G1 == -INFINITY ? 0.f : fast_exp2(pm[r].y - G1);
-        S0 += w0 * pm[r].z;
-        S1 += w1 * pm[r].w;
-        out4[0] += w0 * pv[r].x;
-        out4[1] += w1 * pv[r].y;
-        out4[2] += w0 * pv[r].z;
-        out4[3] += w1 * pv[r].w;
-    }
-    const float inv0 = S0 > 0.f ? __fdividef(vs, S0) : 0.f;
-    const float inv1 = S1 > 0.f ? __fdividef(vs, S1) : 0.f;
-    store_chunk(ob, t.idx + g * K, out4, inv0, inv1, p.group, lane);
     return true;
 }
 
@@ -734,6 +741,7 @@ __device__ int scan_lengths(const Params& p, bool paged, int* sm_pre, int* sm_le
     const int per = (rows + NT - 1) / NT;
     bool bad_len = false;
     int sum = 0;
+#pragma unroll 1
     for (int i = 0; i < per; ++i) {
         const int r = tid * per + i;
         if (r < rows) {
@@ -752,15 +760,10 @@ __device__ int scan_lengths(const Params& p, bool paged, int* sm_pre, int* sm_le
     if (bad_len && flag) flag_error(p.dev_err, PKV_DEV_ERR_SEQ_LEN);
     __syncthreads();
     if (tid < 32) {
-        constexpr int kPer = (NT + 31) / 32;
-        int v[kPer];
+        constexpr int kPer = (NT + 31) / 32;  // partials per lane
         int acc = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int idx = lane * kPer + j;
-            v[j] = idx < NT ? sm_part[idx] : 0;
-            acc += v[j];
-        }
+#pragma unroll 1
+        for (int j = 0; j < kPer; ++j) acc += sm_part[lane * kPer + j];
         int incl = acc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -768,16 +771,17 @@ __device__ int scan_lengths(const Params& p, bool paged, int* sm_pre, int* sm_le
             if (lane >= o) incl += t;
         }
         int run = incl - acc;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < kPer; ++j) {
-            const int idx = lane * kPer + j;
-            if (idx < NT) sm_part[idx] = run;
-            run += v[j];
+            const int v = sm_part[lane * kPer + j];
+            sm_part[lane * kPer + j] = run;
+            run += v;
         }
     }
     __syncthreads();
     {
         int run = sm_part[tid];
+#pragma unroll 1
         for (int i = 0; i < per; ++i) {
             const int r = tid * per + i;
             if (r < rows) {
@@ -814,6 +818,7 @@ __device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int
     if (fits && lane < ng) {
         const int gg = g0 + lane;
         int lo = 0, hi = rows - 1;
+#pragma unroll 1
         while (lo < hi) {  // largest row with sm_pre[row] <= gg
             const int mid = (lo + hi + 1) >> 1;
             if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
@@ -888,6 +893,7 @@ __device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int
     // deal the consumer warps: lane k < np holds piece k
     const int sz = lane < np ? bp->psize[lane] : 0;
     int wc = lane < np ? 1 : 0;
+#pragma unroll 1
     for (int e = np; e < kConsumerWarps; ++e) {
         const int c = lane < np ? (sz + wc - 1) / wc : 0;
         int best = c;
@@ -908,6 +914,7 @@ __device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int
         bp->pw0[lane] = w0;
         bp->pwn[lane] = wc;
         const int a = bp->pfirst[lane];
+#pragma unroll 1
         for (int j = 0; j < wc; ++j) {
             bp->wpiece[w0 + j] = lane;
             bp->wa[w0 + j] = a + j * sz / wc;
@@ -918,6 +925,7 @@ __device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int
     if (lane == 0) {
         // split pieces: a contiguous range has at most two, its first and its last
         int nt = 0;
+#pragma unroll 1
         for (int k = 0; k < np; ++k) {
             if (bp->pP[k] == 1 || nt == kMaxTasks) continue;
             Task& t = bp->tasks[nt++];
@@ -978,36 +986,410 @@ __device__ void row_work(const Params& p, int cta, int G, int lane) {
     }
 }
 
+// Shared-memory views of a decode block, handed to the out-of-line stream
+// functions.
+struct Ctx {
+    unsigned char* smem;
+    uint32_t sbase, bar_full, bar_empty;
+    BlockPlan* bp;
+    volatile int* flags;
+    TileDesc* desc;
+    int* pre;   // granule prefix over rows
+    int* len;   // clamped lengths
+    int* ppos;  // append positions of the block's first pieces
+    const float* ks;  // FP8 scales (shared memory)
+    const float* vs;
+    int W, Geff;
+};
+
+// Stream mode, producer warp: walks the block's range in tiles of up to four
+// granules of one unit, three stages deep, then does the block's row work and
+// drains its copies.
+template <bool kPaged, bool kFp8>
+__device__ __noinline__ void stream_produce(const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                            const Params& p, const Ctx& cx, int cta, int lane) {
+    constexpr uint32_t kGranuleLoad = kFp8 ? 2 * kBoxBytes : kSlotBytes;
+    const BlockPlan* bp = cx.bp;
+    const int g0 = bp->g0, g1 = bp->g1, rows = p.rows, hk = p.hk, G = gridDim.x;
+    const int* sm_pre = cx.pre;
+    const int* sm_len = cx.len;
+    TileDesc* sm_desc = cx.desc;
+    const uint32_t sbase = cx.sbase, bar_full = cx.bar_full, bar_empty = cx.bar_empty;
+    int tile = 0;
+    bool waited = false;
+    bool aborted = false;
+    const uint32_t qbytes = (uint32_t)p.group * 256u;
+    // Stages armed before the dependency wait get their query copies
+    // after it (the query may be written by the preceding kernel).
+    auto wait_and_flush = [&]() {
+        if (waited) return;
+        griddep_wait();
+        waited = true;
+        if (lane == 0)
+            for (int t = 0; t < tile && t < kStages; ++t) {
+                const TileDesc* d = sm_desc + t;
+                if (d->flags & kFirst)
+                    bulk_load(sbase + Smem::q + t * kQBytes,
+                              p.q + ((int64_t)d->r * p.hq + d->kvh * p.group) * kHeadDim, qbytes,
+                              bar_full + 8 * t);
+            }
+    };
+    for (int bg = g0; bg < g1 && !aborted; bg += 32) {
+        const int nbat = min(32, g1 - bg);
+        // Lane j resolves granule bg + j: unit, valid tokens, physical row.
+        int u = -1, r = 0, kvh = 0, n = 1, ustart = 0, tok = 0, valid = 0, zrow = 0;
+        bool issue = false;
+        if (lane < nbat) {
+            const int gg = bg + lane;
+            int lo = 0, hi = rows - 1;
+            while (lo < hi) {  // largest row with sm_pre[row] <= gg
+                const int mid = (lo + hi + 1) >> 1;
+                if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
+            }
+            r = lo;
+            n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+            kvh = (gg - sm_pre[r]) / n;
+            ustart = sm_pre[r] + kvh * n;
+            u = r * hk + kvh;
+            tok = (gg - ustart) * kGranule;
+            valid = min(kGranule, sm_len[r] - tok);
+            if (valid < 0) valid = 0;
+            if (kPaged) {
+                const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
+                if (pb < 0 || pb >= p.nb) {
+                    flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+                    valid = 0;
+                } else {
+                    zrow = pb * p.bs + tok % p.bs;
+                    issue = true;
+                }
+            } else {
+                zrow = r * p.width + tok;
+                issue = true;
+            }
+        }
+        int j = 0;
+        while (j < nbat) {
+            // A tile: up to 4 consecutive granules of one unit.
+            const int uj = __shfl_sync(0xffffffffu, u, j);
+            const unsigned same = __ballot_sync(0xffffffffu, lane < nbat && u == uj) >> j;
+            const unsigned gap = ~same;
+            int ng = gap == 0 ? 32 : __ffs(gap) - 1;
+            ng = min(min(ng, kTileGranules), nbat - j);
+            const int r_j = __shfl_sync(0xffffffffu, r, j);
+            const int kvh_j = __shfl_sync(0xffffffffu, kvh, j);
+            const int n_j = __shfl_sync(0xffffffffu, n, j);
+            const int us_j = __shfl_sync(0xffffffffu, ustart, j);
+            const int tok_j = __shfl_sync(0xffffffffu, tok, j);
+            const int gstart = bg + j;
+            const int pend = min(g1, us_j + n_j);
+            const int pstart = max(g0, us_j);
+            const bool first = gstart == pstart;
+            const bool last = gstart + ng == pend;
+            if (!waited && tile >= kStages) wait_and_flush();
+            const int s = tile % kStages;
+            const uint32_t round = (uint32_t)tile / kStages;
+            if (!mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
+                if (lane == 0) {
+                    cx.flags[0] = 1;
+                    flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+                }
+                aborted = true;
+                break;
+            }
+            const bool mine = lane >= j && lane < j + ng;
+            TileDesc* d = sm_desc + s;
+            if (lane == 0) {
+                d->ustart = us_j;
+                d->pend = pend;
+                d->flags = (first ? kFirst : 0) | (last ? kLast : 0) |
+                           (last && pend == g1 ? kBlockLast : 0);
+                d->r = r_j;
+                d->kvh = kvh_j;
+                d->ng = ng;
+                d->tok0 = tok_j;
+                d->n = n_j;
+            }
+            if (lane < kTileGranules && lane >= ng) d->valid[lane] = 0;
+            if (mine) d->valid[lane - j] = valid;
+            const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, mine && issue));
+            __syncwarp();
+            const uint32_t fb = bar_full + 8 * s;
+            if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kGranuleLoad + (first ? qbytes : 0u));
+            __syncwarp();
+            if (mine && issue) {
+                const uint32_t dst = sbase + Smem::ring + (s * kTileGranules + lane - j) * kSlotBytes;
+                if (kFp8) {
+                    tma_load_3d(dst, kmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kBoxBytes, vmap, 0, kvh, zrow, fb);
+                } else {
+                    tma_load_3d(dst, kmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kBoxBytes, kmap, 64, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV, vmap, 0, kvh, zrow, fb);
+                    tma_load_3d(dst + kSlotV + kBoxBytes, vmap, 64, kvh, zrow, fb);
+                }
+            }
+            if (first && lane == 0 && waited)
+                bulk_load(sbase + Smem::q + s * kQBytes,
+                          p.q + ((int64_t)r_j * p.hq + kvh_j * p.group) * kHeadDim, qbytes, fb);
+            ++tile;
+            j += ng;
+        }
+    }
+    wait_and_flush();
+    if (!aborted) {
+        // End marker: an empty stage whose descriptor says "no more tiles".
+        const int s = tile % kStages;
+        const uint32_t round = (uint32_t)tile / kStages;
+        if (mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
+            if (lane == 0) {
+                sm_desc[s].flags = kEnd;
+                mbar_arrive(bar_full + 8 * s);
+            }
+            ++tile;
+        } else if (lane == 0) {
+            cx.flags[0] = 1;
+            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+        }
+    }
+    if (kPaged) row_work<kFp8>(p, cta, G, lane);
+    // Drain: the copies of every armed stage land before the block exits.
+    for (int t = tile - kStages; t < tile; ++t) {
+        if (t < 0) continue;
+        if (!mbar_wait(bar_full + 8 * (t % kStages), (uint32_t)(t / kStages) & 1) && lane == 0)
+            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+    }
+}
+
+// Stream mode, consumer warps 0-3: one granule per warp per stage; at each
+// piece's end the four warps dump their states and combine them.  Records the
+// block's split pieces as merge tasks.
+template <bool kPaged, bool kFp8>
+__device__ __noinline__ void stream_consume(const Params& p, const Ctx& cx, int cta, int warp,
+                                            int lane) {
+    const int tid = threadIdx.x, rows = p.rows, hk = p.hk;
+    const BlockPlan* bpc = cx.bp;
+    BlockPlan* bp = cx.bp;
+    const int g0 = bpc->g0, g1 = bpc->g1;
+    const int* sm_pre = cx.pre;
+    int* sm_ppos = cx.ppos;
+    volatile int* sm_flags = cx.flags;
+    unsigned char* smem = cx.smem;
+    const uint32_t sbase = cx.sbase, bar_full = cx.bar_full, bar_empty = cx.bar_empty;
+    const bool fused = kPaged && p.positions != nullptr;
+    const int gq = lane >> 2, tq = lane & 3;
+    // Append positions of this block's first pieces, read once right after
+    // the wait, so a piece never starts with a dependent global load.
+    if (fused) {
+        if (tid == 0) {
+            int lo = 0, hi = rows - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
+            }
+            int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+            int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n, k = 0;
+            for (int g = g0; g < g1 && k < kMaxPieces;) {
+                sm_ppos[k++] = r;  // row of piece k (replaced by its position below)
+                g = min(g1, us + n);
+                if (g >= g1) break;
+                if (kvh + 1 < hk) {
+                    ++kvh;
+                    us += n;
+                } else {
+                    ++r;
+                    while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
+                    kvh = 0;
+                    n = (sm_pre[r + 1] - sm_pre[r]) / hk;
+                    us = sm_pre[r];
+                }
+            }
+            sm_flags[2] = k;
+        }
+        named_sync(kBarStream, kStreamWarps * 32);
+    }
+    // Each thread's position load stays in flight while the first tile lands;
+    // it is published to shared memory after the first full barrier.
+    const int npp = fused ? sm_flags[2] : 0;
+    const int my_pos = tid < npp ? p.positions[sm_ppos[tid]] : 0;
+    bool pos_published = !fused;
+    int piece = 0;
+
+    uint32_t qb[16];
+    Soft st;
+    st.reset();
+    int patch_tok = -1;  // unit-local token this piece must take from k_new / v_new
+    uint4 patch_val = make_uint4(0, 0, 0, 0);
+    int tile = 0;
+    while (true) {
+        const int s = tile % kStages;
+        const uint32_t round = (uint32_t)tile / kStages;
+        if (!mbar_wait(bar_full + 8 * s, round & 1)) {
+            if (lane == 0) {
+                sm_flags[0] = 1;
+                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            }
+            break;
+        }
+        if (!pos_published) {
+            if (tid < npp) sm_ppos[tid] = my_pos;
+            named_sync(kBarStream, kStreamWarps * 32);
+            pos_published = true;
+        }
+        const TileDesc* d = cx.desc + s;
+        const int flags = d->flags;
+        if (flags & kEnd) break;
+        const int r = d->r, kvh = d->kvh, ng = d->ng, tok0 = d->tok0;
+        const int ustart = d->ustart, n = d->n, pend = d->pend;
+        const int valid = warp < ng ? d->valid[warp] : 0;
+        if (flags & kFirst) {
+            load_q(qb, reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256),
+                   gq < p.group, tq);
+            st.reset();
+            patch_tok = -1;
+            const int this_piece = piece++;
+            if (fused) {
+                // The appended token, if it falls inside this piece, is taken from
+                // k_new / v_new (its slot may be written concurrently).
+                const int pos = this_piece < kMaxPieces ? sm_ppos[this_piece] : p.positions[r];
+                const int pg = pos >= 0 ? ustart + pos / kGranule : -1;
+                if (pos >= 0 && pg >= ustart + tok0 / kGranule && pg < pend) {
+                    patch_tok = pos;
+                    const int chunk = lane & 15;
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
+                    patch_val = src[chunk];
+                    if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? cx.ks[kvh] : cx.vs[kvh]));
+                }
+            }
+        }
+        bool wrote = false;
+        if (warp < ng) {
+            const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
+            const int si = s * kTileGranules + warp;
+            if (kFp8) widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
+            wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
+                                           patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
+            if (wrote) __syncwarp();
+            attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid,
+                   kFp8 ? p.scale_log2 * cx.ks[kvh] : p.scale_log2, lane);
+        }
+        ++tile;
+        if (!(flags & kLast)) {
+            // Generic-proxy writes must be ordered before TMA reuses the slot.
+            if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            continue;
+        }
+
+        // ---- end of a piece: the four warps dump their states into their
+        // slots of this stage, which stays held until every warp has
+        // read them; warp j combines chunks j and j + 4 of all four ----
+        st.reduce_l();
+        __syncwarp();
+        dump_state(st, smem + Smem::ring + (s * kTileGranules + warp) * kSlotBytes, lane);
+        named_sync(kBarStream, kStreamWarps * 32);
+        const int cs = owner_of(ustart, cx.W, cx.Geff);
+        const int P = owner_of(ustart + n - 1, cx.W, cx.Geff) - cs + 1;
+        {
+            const PieceOut po = piece_out(p, r, kvh, cs, P, cta, kFp8 ? cx.vs[kvh] : 1.f);
+            combine_dumps(po, smem + Smem::ring, nullptr, s * kTileGranules, kStreamWarps, warp, lane);
+        }
+        // Generic-proxy writes must be ordered before TMA reuses the slots.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (P > 1 && tid == 0) {
+            // A contiguous range has at most two split pieces: its first and its last.
+            const int k = bp->ntasks;
+            if (k < kMaxTasks) {
+                Task& t = bp->tasks[k];
+                t.u = r * hk + kvh;
+                t.cs = cs;
+                t.P = P;
+                t.idx = cta - cs;
+                t.r = r;
+                t.kvh = kvh;
+                bp->ntasks = k + 1;
+            }
+        }
+    }
+    // the ring is idle once every stage is consumed
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    named_sync(kBarStream, kStreamWarps * 32);
+}
+
+// Burst mode, warp j of piece k's n warps (n > 1): chunks c = j, j + n, ...
+// of the piece.  Combines the states the piece's warps dumped into their
+// first slots through their log-sum-exp and emits each chunk (fp16 output of
+// a whole unit, or the piece's record); warp 0 also emits a split piece's m/l.
+__device__ void burst_emit(const PieceOut& po, const BlockPlan* bp, const unsigned char* ring, int k,
+                           int j, int lane) {
+    const int n = bp->pwn[k], w0 = bp->pw0[k], g0 = bp->g0, tq = lane & 3;
+    uint32_t off[kConsumerWarps];
+    float4 ml[kConsumerWarps];
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s) {
+        off[s] = (uint32_t)(bp->wa[w0 + (s < n ? s : 0)] - g0) * kSlotBytes;
+        ml[s] = *reinterpret_cast<const float4*>(ring + off[s] + 16 * tq);
+    }
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s)
+        if (s < n) {
+            M0 = fmaxf(M0, ml[s].x);
+            M1 = fmaxf(M1, ml[s].y);
+        }
+    float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+    for (int s = 0; s < kConsumerWarps; ++s) {  // ml[s].x / .y become the weights
+        ml[s].x = s < n && M0 != -INFINITY ? fast_exp2(ml[s].x - M0) : 0.f;
+        ml[s].y = s < n && M1 != -INFINITY ? fast_exp2(ml[s].y - M1) : 0.f;
+        L0 += ml[s].x * ml[s].z;
+        L1 += ml[s].y * ml[s].w;
+    }
+#pragma unroll 1
+    for (int c = j; c < 8; c += n) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < kConsumerWarps; ++s) {
+            const float4 v = *reinterpret_cast<const float4*>(ring + off[s] + kMlBytes + c * kChunkBytes + lane * 16);
+            acc[0] += ml[s].x * v.x;
+            acc[1] += ml[s].y * v.y;
+            acc[2] += ml[s].x * v.z;
+            acc[3] += ml[s].y * v.w;
+        }
+        emit_chunk(po, c, acc, L0, L1, lane);
+    }
+    if (j == 0) emit_ml(po, M0, M1, L0, L1, lane);
+}
+
 template <bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_tma_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const Params p) {
+                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ Params prm) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Params& p = prm;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + Smem::bars;
     const uint32_t bar_empty = bar_full + kStages * 8;
     const uint32_t bar_slot = bar_full + 2 * kStages * 8;
-    int* sm_ppos = reinterpret_cast<int*>(smem + Smem::ppos);
-    TileDesc* sm_desc = reinterpret_cast<TileDesc*>(smem + Smem::desc);
     BlockPlan* bp = reinterpret_cast<BlockPlan*>(smem + Smem::plan);
     volatile int* sm_flags = reinterpret_cast<volatile int*>(smem + Smem::flags);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
     int* sm_pre = reinterpret_cast<int*>(smem + Smem::prefix);
-    int* sm_len = reinterpret_cast<int*>(smem + Smem::lens(p.rows));
+    int* sm_len = reinterpret_cast<int*>(smem + Smem::lens(prm.rows));
     float* sm_ks = reinterpret_cast<float*>(smem + Smem::scales);  // FP8 only
     float* sm_vs = sm_ks + kFp8MaxKvHeads;
-    // bytes the producer lands per granule
-    constexpr uint32_t kGranuleLoad = kFp8 ? 2 * kBoxBytes : kSlotBytes;
-
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int G = gridDim.x;
     const int cta = blockIdx.x;
-    const int hk = p.hk;
-    const int rows = p.rows;
+    const int hk = prm.hk;
 
     // The next kernel in the stream (launched with programmatic stream
     // serialization) may be scheduled as soon as every block has started:
@@ -1022,9 +1404,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
         }
         // the step's plan for this block: one 16-byte load per lane
-        if (p.plan)
+        if (prm.plan)
             reinterpret_cast<uint4*>(bp)[lane] =
-                __ldg(reinterpret_cast<const uint4*>(p.plan + (size_t)cta * kPlanBytes) + lane);
+                __ldg(reinterpret_cast<const uint4*>(prm.plan + (size_t)cta * kPlanBytes) + lane);
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -1037,8 +1419,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         sm_flags[0] = 0;  // abort
         sm_flags[4] = sm_flags[5] = 0;  // a merge task's poll gave up
     }
-    if (kFp8 && tid < 2 * p.hk) sm_ks[tid < p.hk ? tid : kFp8MaxKvHeads + tid - p.hk] =
-        tid < p.hk ? p.k_scale[tid] : p.v_scale[tid - p.hk];
+    if (kFp8 && tid < 2 * hk) sm_ks[tid < hk ? tid : kFp8MaxKvHeads + tid - hk] =
+        tid < hk ? prm.k_scale[tid] : prm.v_scale[tid - hk];
     __syncthreads();
 
     // ---- the block's plan: loaded (made for this grid), or made here ----
@@ -1060,234 +1442,81 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int mode = bp->mode;
     const int g0 = bp->g0, g1 = bp->g1;
+    Ctx cx;
+    cx.smem = smem;
+    cx.sbase = sbase;
+    cx.bar_full = bar_full;
+    cx.bar_empty = bar_empty;
+    cx.bp = bp;
+    cx.flags = sm_flags;
+    cx.desc = reinterpret_cast<TileDesc*>(smem + Smem::desc);
+    cx.pre = sm_pre;
+    cx.len = sm_len;
+    cx.ppos = reinterpret_cast<int*>(smem + Smem::ppos);
+    cx.ks = sm_ks;
+    cx.vs = sm_vs;
+    cx.W = W;
+    cx.Geff = Geff;
 
     if (warp == kConsumerWarps) {
         // ============================ producer ============================
-        if (mode == kModeIdle) {
-            griddep_wait();
-            if (kPaged) row_work<kFp8>(p, cta, G, lane);
+        if (mode == kModeStream) {
+            stream_produce<kPaged, kFp8>(&kmap, &vmap, p, cx, cta, lane);
             return;
         }
-        if (mode == kModeBurst) {
-            // Every granule of the range goes to its own slot now, before the
-            // dependency wait; lane j handles granule g0 + j.
-            const int ng = g1 - g0;
-            if (lane < ng) {
-                const int zrow = bp->szrow[lane], kvh = bp->skvh[lane];
-                const uint32_t fb = bar_slot + 8 * lane;
-                mbar_arrive_expect_tx(fb, zrow >= 0 ? kGranuleLoad : 0u);
-                if (zrow >= 0) {
-                    const uint32_t dst = sbase + Smem::ring + lane * kSlotBytes;
-                    if (kFp8) {
-                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kBoxBytes, &vmap, 0, kvh, zrow, fb);
-                    } else {
-                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
-                        tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
-                    }
-                }
-            }
-            griddep_wait();
-            if (kPaged) row_work<kFp8>(p, cta, G, lane);
-            // Drain: every copy lands before the block exits.
-#pragma unroll 1
-            for (int j = 0; j < ng; ++j)
-                if (!mbar_wait(bar_slot + 8 * j, 0) && lane == 0) flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            return;
-        }
-        int tile = 0;
-        bool waited = false;
-        bool aborted = false;
-        const uint32_t qbytes = (uint32_t)p.group * 256u;
-        // Stages armed before the dependency wait get their query copies
-        // after it (the query may be written by the preceding kernel).
-        auto wait_and_flush = [&]() {
-            if (waited) return;
-            griddep_wait();
-            waited = true;
-            if (lane == 0)
-                for (int t = 0; t < tile && t < kStages; ++t) {
-                    const TileDesc* d = sm_desc + t;
-                    if (d->flags & kFirst)
-                        bulk_load(sbase + Smem::q + t * kQBytes,
-                                  p.q + ((int64_t)d->r * p.hq + d->kvh * p.group) * kHeadDim, qbytes,
-                                  bar_full + 8 * t);
-                }
-        };
-        for (int bg = g0; bg < g1 && !aborted; bg += 32) {
-            const int nbat = min(32, g1 - bg);
-            // Lane j resolves granule bg + j: unit, valid tokens, physical row.
-            int u = -1, r = 0, kvh = 0, n = 1, ustart = 0, tok = 0, valid = 0, zrow = 0;
-            bool issue = false;
-            if (lane < nbat) {
-                const int gg = bg + lane;
-                int lo = 0, hi = rows - 1;
-                while (lo < hi) {  // largest row with sm_pre[row] <= gg
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
-                }
-                r = lo;
-                n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                kvh = (gg - sm_pre[r]) / n;
-                ustart = sm_pre[r] + kvh * n;
-                u = r * hk + kvh;
-                tok = (gg - ustart) * kGranule;
-                valid = min(kGranule, sm_len[r] - tok);
-                if (valid < 0) valid = 0;
-                if (kPaged) {
-                    const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
-                    if (pb < 0 || pb >= p.nb) {
-                        flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-                        valid = 0;
-                    } else {
-                        zrow = pb * p.bs + tok % p.bs;
-                        issue = true;
-                    }
-                } else {
-                    zrow = r * p.width + tok;
-                    issue = true;
-                }
-            }
-            int j = 0;
-            while (j < nbat) {
-                // A tile: up to 4 consecutive granules of one unit.
-                const int uj = __shfl_sync(0xffffffffu, u, j);
-                const unsigned same = __ballot_sync(0xffffffffu, lane < nbat && u == uj) >> j;
-                const unsigned gap = ~same;
-                int ng = gap == 0 ? 32 : __ffs(gap) - 1;
-                ng = min(min(ng, kTileGranules), nbat - j);
-                const int r_j = __shfl_sync(0xffffffffu, r, j);
-                const int kvh_j = __shfl_sync(0xffffffffu, kvh, j);
-                const int n_j = __shfl_sync(0xffffffffu, n, j);
-                const int us_j = __shfl_sync(0xffffffffu, ustart, j);
-                const int tok_j = __shfl_sync(0xffffffffu, tok, j);
-                const int gstart = bg + j;
-                const int pend = min(g1, us_j + n_j);
-                const int pstart = max(g0, us_j);
-                const bool first = gstart == pstart;
-                const bool last = gstart + ng == pend;
-                if (!waited && tile >= kStages) wait_and_flush();
-                const int s = tile % kStages;
-                const uint32_t round = (uint32_t)tile / kStages;
-                if (!mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
-                    if (lane == 0) {
-                        sm_flags[0] = 1;
-                        flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                    }
-                    aborted = true;
-                    break;
-                }
-                const bool mine = lane >= j && lane < j + ng;
-                TileDesc* d = sm_desc + s;
-                if (lane == 0) {
-                    d->ustart = us_j;
-                    d->pend = pend;
-                    d->flags = (first ? kFirst : 0) | (last ? kLast : 0) |
-                               (last && pend == g1 ? kBlockLast : 0);
-                    d->r = r_j;
-                    d->kvh = kvh_j;
-                    d->ng = ng;
-                    d->tok0 = tok_j;
-                    d->n = n_j;
-                }
-                if (lane < kTileGranules && lane >= ng) d->valid[lane] = 0;
-                if (mine) d->valid[lane - j] = valid;
-                const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, mine && issue));
-                __syncwarp();
-                const uint32_t fb = bar_full + 8 * s;
-                if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kGranuleLoad + (first ? qbytes : 0u));
-                __syncwarp();
-                if (mine && issue) {
-                    const uint32_t dst =
-                        sbase + Smem::ring + (s * kTileGranules + lane - j) * kSlotBytes;
-                    if (kFp8) {
-                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kBoxBytes, &vmap, 0, kvh, zrow, fb);
-                    } else {
-                        tma_load_3d(dst, &kmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kBoxBytes, &kmap, 64, kvh, zrow, fb);
-                        tma_load_3d(dst + kSlotV, &vmap, 0, kvh, zrow, fb);
-                        tma_load_3d(dst + kSlotV + kBoxBytes, &vmap, 64, kvh, zrow, fb);
-                    }
-                }
-                if (first && lane == 0 && waited)
-                    bulk_load(sbase + Smem::q + s * kQBytes,
-                              p.q + ((int64_t)r_j * p.hq + kvh_j * p.group) * kHeadDim, qbytes, fb);
-                ++tile;
-                j += ng;
-            }
-        }
-        wait_and_flush();
-        if (!aborted) {
-            // End marker: an empty stage whose descriptor says "no more tiles".
-            const int s = tile % kStages;
-            const uint32_t round = (uint32_t)tile / kStages;
-            if (mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
-                if (lane == 0) {
-                    sm_desc[s].flags = kEnd;
-                    mbar_arrive(bar_full + 8 * s);
-                }
-                ++tile;
-            } else if (lane == 0) {
-                sm_flags[0] = 1;
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            }
-        }
+        // Burst (or idle): the consumer warps stage their own granules; this
+        // warp only does the block's row work after the dependency wait.
+        griddep_wait();
         if (kPaged) row_work<kFp8>(p, cta, G, lane);
-        // Drain: the copies of every armed stage land before the block exits.
-        for (int t = tile - kStages; t < tile; ++t) {
-            if (t < 0) continue;
-            if (!mbar_wait(bar_full + 8 * (t % kStages), (uint32_t)(t / kStages) & 1) && lane == 0)
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-        }
         return;
     }
 
     // ============================== consumers ==============================
-    const bool burst = mode == kModeBurst;
-    if (!burst && warp >= kStreamWarps) return;  // stream mode runs on warps 0-3
-    if (burst && bp->wpiece[warp] >= 0) {
-        // Warm L2 with this warp's query rows and new token.  A prefetch reads
-        // nothing into the block, so it may precede the dependency wait: the
-        // values used are loaded after it.
-        const int pi = bp->wpiece[warp];
-        const int r = bp->pr[pi], kvh = bp->pkvh[pi];
-        const char* qrow = reinterpret_cast<const char*>(p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim);
-        if (lane < 2 * p.group)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lane * 128));
-        if (kPaged && p.positions && lane < 8) {
-            const char* nt = reinterpret_cast<const char*>(
-                (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
-        }
-    }
-    // Everything below may read what the preceding kernel wrote (query,
-    // positions, new tokens, workspace) or write what it reads.
-    griddep_wait();
-
-    if (mode == kModeIdle) return;
-
-    const bool fused = kPaged && p.positions != nullptr;
-    const int gq = lane >> 2;  // MMA group id: token row (QK) / dim row (PV) / head (B frag)
-    const int tq = lane & 3;   // thread in group
-
-    if (burst) {
+    if (mode == kModeStream) {
+        if (warp >= kStreamWarps) return;  // stream mode runs on warps 0-3
+        griddep_wait();
+        stream_consume<kPaged, kFp8>(p, cx, cta, warp, lane);
+    } else {
         // ============================ burst mode ============================
         const int pi = bp->wpiece[warp];
-        Soft st;
-        st.reset();
-        bool ok = true;
-        int r = 0, kvh = 0;
         if (pi >= 0) {
-            r = bp->pr[pi];
-            kvh = bp->pkvh[pi];
-            const int us = bp->pus[pi];
+            // This warp's granules go to their slots now, before the
+            // dependency wait (the cached tokens are not written by the
+            // preceding kernel; the appended one is patched in after it).
+            const unsigned char* kpool = reinterpret_cast<const unsigned char*>(kmap_base(p, false));
+            const unsigned char* vpool = reinterpret_cast<const unsigned char*>(kmap_base(p, true));
+#pragma unroll 1
+            for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g) {
+                const int si = g - g0, zrow = bp->szrow[si];
+                stage_granule<kFp8>(sbase + Smem::ring + si * kSlotBytes, kpool, vpool, zrow < 0 ? 0 : zrow, hk,
+                                    bp->skvh[si], zrow < 0 ? 0 : bp->svalid[si], lane);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            // Warm L2 with this warp's query rows and new token.  A prefetch
+            // reads nothing into the block, so it may precede the dependency
+            // wait: the values used are loaded after it.
+            const int r = bp->pr[pi], kvh = bp->pkvh[pi];
+            const char* qrow = reinterpret_cast<const char*>(p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim);
+            if (lane < 2 * p.group)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lane * 128));
+            if (kPaged && p.positions && lane < 8) {
+                const char* nt = reinterpret_cast<const char*>(
+                    (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
+            }
+        }
+        // Everything below may read what the preceding kernel wrote (query,
+        // positions, new tokens, workspace) or write what it reads.
+        griddep_wait();
+        if (mode == kModeIdle) return;
+        const bool fused = kPaged && p.positions != nullptr;
+        if (pi >= 0) {
+            Soft st;
+            st.reset();
+            const int r = bp->pr[pi], kvh = bp->pkvh[pi], us = bp->pus[pi];
             const int a = bp->wa[warp], b = bp->wb[warp];
             uint32_t qb[16];
-            load_q(qb, reinterpret_cast<const uint32_t*>(p.q + ((int64_t)r * p.hq + kvh * p.group + gq) * kHeadDim),
-                   gq < p.group, tq);
+            load_q_global(qb, p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim, p.group, lane);
             // The appended token, if it falls inside this warp's granules, is
             // taken from k_new / v_new (its slot may be written concurrently).
             int patch_tok = -1;
@@ -1302,28 +1531,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
             }
             const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
+            const bool ok = true;
+            // this lane's copies have landed; then every lane's
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            __syncwarp();
 #pragma unroll 1
             for (int g = a; g < b; ++g) {
                 const int si = g - g0;
-                if (!mbar_wait(bar_slot + 8 * si, 0)) {
-                    if (lane == 0) {
-                        sm_flags[0] = 1;
-                        flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                    }
-                    ok = false;
-                    break;
-                }
-                const int valid = bp->svalid[si];
                 unsigned char* sp = smem + Smem::ring + si * kSlotBytes;
-                bool wrote = false;
-                if (kFp8) {
-                    widen_fp8_slot(sp, lane);
-                    wrote = true;
+                if (kFp8) widen_fp8_slot(sp, lane);
+                const int prow = patch_tok >= 0 ? patch_tok - (g - us) * kGranule : -1;
+                if (prow >= 0 && prow < bp->svalid[si]) {
+                    // the appended token's row, in the fp16 slot layout
+                    const int c16 = lane & 15;  // 16-byte chunk of the 128 dims
+                    unsigned char* box = sp + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
+                    *reinterpret_cast<uint4*>(box + prow * 128 + (((c16 & 7) ^ (prow & 7)) << 4)) = patch_val;
                 }
-                const int gtok = (g - us) * kGranule;
-                wrote |= prepare_granule(sp, valid, patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
-                if (wrote) __syncwarp();
-                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid, sl2, lane);
+                __syncwarp();
+                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, bp->svalid[si], sl2, lane);
             }
             st.reduce_l();
             __syncwarp();
@@ -1336,161 +1561,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 named_sync(kBarPiece + pi, k * 32);
             }
             if (!sm_flags[0]) {
-                const int cs = bp->pcs[pi];
-                const PieceOut po = piece_out(p, r, kvh, cs, bp->pP[pi], cta, kFp8 ? sm_vs[kvh] : 1.f);
+                const PieceOut po = piece_out(p, r, kvh, bp->pcs[pi], bp->pP[pi], cta, kFp8 ? sm_vs[kvh] : 1.f);
                 if (k == 1) {
-                    finish_own(po, st, lane);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) emit_chunk(po, c, st.o[c], st.l0, st.l1, lane);
+                    emit_ml(po, st.m0, st.m1, st.l0, st.l1, lane);
                 } else {
-                    const int w0 = bp->pw0[pi];
-                    combine_dumps(po, smem + Smem::ring, bp->wa + w0, g0, k, warp - w0, lane);
+                    burst_emit(po, bp, smem + Smem::ring, pi, warp - bp->pw0[pi], lane);
                 }
             }
         }
         // every dump has been read: the ring is free for the merges
         named_sync(kBarConsumers, kConsumers);
-    } else {
-        // ============================ stream mode ============================
-        // Append positions of this block's first pieces, read once right after
-        // the wait, so a piece never starts with a dependent global load.
-        if (fused) {
-            if (tid == 0) {
-                int lo = 0, hi = rows - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
-                }
-                int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n, k = 0;
-                for (int g = g0; g < g1 && k < kMaxPieces;) {
-                    sm_ppos[k++] = r;  // row of piece k (replaced by its position below)
-                    g = min(g1, us + n);
-                    if (g >= g1) break;
-                    if (kvh + 1 < hk) {
-                        ++kvh;
-                        us += n;
-                    } else {
-                        ++r;
-                        while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
-                        kvh = 0;
-                        n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                        us = sm_pre[r];
-                    }
-                }
-                sm_flags[2] = k;
-            }
-            named_sync(kBarStream, kStreamWarps * 32);
-        }
-        // Each thread's position load stays in flight while the first tile lands;
-        // it is published to shared memory after the first full barrier.
-        const int npp = fused ? sm_flags[2] : 0;
-        const int my_pos = tid < npp ? p.positions[sm_ppos[tid]] : 0;
-        bool pos_published = !fused;
-        int piece = 0;
-
-        uint32_t qb[16];
-        Soft st;
-        st.reset();
-        int patch_tok = -1;        // unit-local token this piece must take from k_new / v_new
-        uint4 patch_val = make_uint4(0, 0, 0, 0);
-        int tile = 0;
-        while (true) {
-            const int s = tile % kStages;
-            const uint32_t round = (uint32_t)tile / kStages;
-            if (!mbar_wait(bar_full + 8 * s, round & 1)) {
-                if (lane == 0) {
-                    sm_flags[0] = 1;
-                    flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                }
-                break;
-            }
-            if (!pos_published) {
-                if (tid < npp) sm_ppos[tid] = my_pos;
-                named_sync(kBarStream, kStreamWarps * 32);
-                pos_published = true;
-            }
-            const TileDesc* d = sm_desc + s;
-            const int flags = d->flags;
-            if (flags & kEnd) break;
-            const int r = d->r, kvh = d->kvh, ng = d->ng, tok0 = d->tok0;
-            const int ustart = d->ustart, n = d->n, pend = d->pend;
-            const int valid = warp < ng ? d->valid[warp] : 0;
-            if (flags & kFirst) {
-                load_q(qb, reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256),
-                       gq < p.group, tq);
-                st.reset();
-                patch_tok = -1;
-                const int this_piece = piece++;
-                if (fused) {
-                    // The appended token, if it falls inside this piece, is taken from
-                    // k_new / v_new (its slot may be written concurrently).
-                    const int pos = this_piece < kMaxPieces ? sm_ppos[this_piece] : p.positions[r];
-                    const int pg = pos >= 0 ? ustart + pos / kGranule : -1;
-                    if (pos >= 0 && pg >= ustart + tok0 / kGranule && pg < pend) {
-                        patch_tok = pos;
-                        const int chunk = lane & 15;
-                        const uint4* src = reinterpret_cast<const uint4*>(
-                            (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
-                        patch_val = src[chunk];
-                        if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
-                    }
-                }
-            }
-            bool wrote = false;
-            if (warp < ng) {
-                const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
-                const int si = s * kTileGranules + warp;
-                if (kFp8) widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
-                wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
-                                               patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
-                if (wrote) __syncwarp();
-                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid,
-                       kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2, lane);
-            }
-            ++tile;
-            if (!(flags & kLast)) {
-                // Generic-proxy writes must be ordered before TMA reuses the slot.
-                if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-                continue;
-            }
-
-            // ---- end of a piece: the four warps dump their states into their
-            // slots of this stage, which stays held until every warp has
-            // read them; warp j combines chunks j and j + 4 of all four ----
-            st.reduce_l();
-            __syncwarp();
-            dump_state(st, smem + Smem::ring + (s * kTileGranules + warp) * kSlotBytes, lane);
-            named_sync(kBarStream, kStreamWarps * 32);
-            const int cs = owner_of(ustart, W, Geff);
-            const int P = owner_of(ustart + n - 1, W, Geff) - cs + 1;
-            {
-                const PieceOut po = piece_out(p, r, kvh, cs, P, cta, kFp8 ? sm_vs[kvh] : 1.f);
-                combine_dumps(po, smem + Smem::ring, nullptr, s * kTileGranules, kStreamWarps, warp,
-                              lane);
-            }
-            // Generic-proxy writes must be ordered before TMA reuses the slots.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-            if (P > 1 && tid == 0) {
-                // A contiguous range has at most two split pieces: its first and its last.
-                const int k = bp->ntasks;
-                if (k < kMaxTasks) {
-                    Task& t = bp->tasks[k];
-                    t.u = r * hk + kvh;
-                    t.cs = cs;
-                    t.P = P;
-                    t.idx = cta - cs;
-                    t.r = r;
-                    t.kvh = kvh;
-                    bp->ntasks = k + 1;
-                }
-            }
-        }
-        // the ring is idle once every stage is consumed
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        named_sync(kBarStream, kStreamWarps * 32);
     }
 
     // ---- merges: the block's split pieces that make it a participant (the
@@ -1508,6 +1590,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     if (ntask == 0) return;
+    const bool burst = mode == kModeBurst;
     const int nc = burst ? kConsumerWarps : kStreamWarps;
     const int half = nc / 2;
     const int t = ntask == 1 ? first : (warp < half ? 0 : 1);
@@ -1705,6 +1788,8 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
 
     prm.k_scale = k_scale;
     prm.v_scale = v_scale;
+    prm.kbase = k_base;
+    prm.vbase = v_base;
 
     const uint32_t smem = Smem::total(rows);
     const int which = fp8 ? 2 : paged ? 0 : 1;
