@@ -51,12 +51,15 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mixed", "uniform"], default="mixed")
+    ap.add_argument("--workload", choices=["mixed", "uniform", "shared", "long", "tiny"],
+                    default="mixed")
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config lines (tiny, uniform, shared, long)")
     return ap.parse_args()
 
 
@@ -216,13 +219,25 @@ def make_case(args):
     from paged_kv_cache_06_gb300 import workloads as wl
     if args.workload == "mixed":
         return wl.mixed(seed=args.seed, layers=args.layers)
-    return wl.uniform(seed=args.seed, layers=args.layers)
+    if args.workload == "uniform":
+        return wl.uniform(seed=args.seed, layers=args.layers)
+    return wl.WORKLOADS[args.workload](seed=args.seed)
+
+
+CONFIG_DESC = {
+    "tiny": "4 rows of 1 / 17 / 64 / 200 tokens, 16-token blocks, one append per row",
+    "uniform": "32 rows x 1024 tokens, 64-token blocks",
+    "mixed": "31 rows U{16..512} + 1 row of 4096, 64-token blocks",
+    "shared": "96 rows log-uniform on [16, 8192], 16-token blocks, the first 592 tokens "
+              "(37 blocks) shared by every row",
+    "long": "4 rows x 32769 tokens (one append at 32768), 64-token blocks",
+}
 
 
 def workload_config(case, args):
     from paged_kv_cache_06_gb300 import workloads as wl
     b = wl.algorithmic_bytes(case)
-    desc = ("31 rows U{16..512} + 1 row of 4096" if args.workload == "mixed" else "32 rows x 1024")
+    desc = CONFIG_DESC[args.workload]
     return {
         "workload": args.workload, "rows": case.rows, "layers": case.layers,
         "lengths": desc, "tokens_per_layer": int(case.seq_lens.sum()),
@@ -262,6 +277,96 @@ def cpu_oracle_sample(case, seconds: float = CPU_SAMPLE_SECONDS, threads: int = 
 
 
 # ---------------------------------------------------------------------------
+
+def measure_configs(args, dev, peak, peak_kind):
+    """Every workload configuration as its own timed step (fused append +
+    decode per launch, programmatic dependent launch between launches, one
+    CUDA graph).  Single-layer configurations are timed over several copies
+    of their pool, one per launch, so that the step reads more than L2 holds
+    (a real model's layers each have their own pool); the tiny one stays in
+    L2 whatever the copies.  The shared-prefix roofline counts each distinct
+    block once (a block that many rows read is served from L2 after its first
+    read); its logical bytes are reported beside it."""
+    import torch
+    from paged_kv_cache_06_gb300 import ops
+    from paged_kv_cache_06_gb300 import workloads as wl
+    copies = {"tiny": 28, "uniform": 1, "shared": 4, "long": 4}
+    out_cfg = {}
+    for name in ("tiny", "uniform", "shared", "long"):
+        if name == "uniform":
+            case = wl.uniform(seed=args.seed, layers=args.layers)
+        else:
+            case = wl.WORKLOADS[name](seed=args.seed)
+        b = wl.algorithmic_bytes(case)
+        d = wl.to_device(case, dev)
+        n = case.layers * copies[name]
+        kp = [d["k_pool"][l % case.layers].clone() if copies[name] > 1 else d["k_pool"][l]
+              for l in range(n)]
+        vp = [d["v_pool"][l % case.layers].clone() if copies[name] > 1 else d["v_pool"][l]
+              for l in range(n)]
+        del d["k_pool"], d["v_pool"]
+        rows, hq, hk, hd = case.rows, case.q_heads, case.kv_heads, case.head_dim
+        ws = ops.alloc_workspace(rows, hq, hk, hd, case.max_seq_len, case.block_size, device=dev)
+        out = torch.zeros(n, rows, hq, hd, dtype=torch.float16, device=dev)
+        has_append = bool((case.positions >= 0).any())
+
+        def step():
+            # positions < 0 (the shared-prefix rows) append nothing
+            for l in range(n):
+                li = l % case.layers
+                ops.append_decode(out[l], d["q"][li], kp[l], vp[l], d["block_tables"],
+                                  d["seq_lens"], d["positions"], d["k_new"][li], d["v_new"][li],
+                                  case.scale, case.max_seq_len, ws, pdl=True)
+
+        step()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                step()
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        per_launch = ms * 1e-3 / n
+        logical = b["decode_layer"] + b["append_layer"]
+        unique = b["decode_layer_unique"] + b["append_layer"]
+        roof_bytes = unique if name == "shared" else logical
+        achieved = roof_bytes / per_launch / 1e9
+        entry = {
+            "workload": CONFIG_DESC[name], "rows": rows, "block_size": case.block_size,
+            "launches_per_step": n, "ms_per_step": round(ms, 5),
+            "us_per_launch": round(per_launch * 1e6, 3),
+            "bytes_per_launch": roof_bytes,
+            "GBps": round(achieved, 2),
+            "rows_layers_per_s": round(rows * n / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_kind},
+            "what": ("append + decode (one fused launch)" if has_append else "decode")
+                    + (f", {copies[name]} pool copies" if copies[name] > 1 else ""),
+        }
+        if name == "shared":
+            entry["kv_logical_bytes"] = b["kv_logical"]
+            entry["kv_unique_bytes"] = b["kv_unique"]
+            entry["GBps_logical"] = round(logical / per_launch / 1e9, 2)
+        if name == "tiny":
+            entry["note"] = "0.29 MB per launch: L2-resident; a launch-latency figure"
+        out_cfg[name] = entry
+        del g, kp, vp, d, out, ws
+        torch.cuda.empty_cache()
+    return out_cfg
+
 
 def run_ours(args, rank, world, pg):
     import torch
@@ -488,6 +593,20 @@ def run_ours(args, rank, world, pg):
         "gpu_launches": args.steps * L,
         "clocks": clk,
     }
+
+    if not args.no_configs and args.workload == "mixed":
+        cfgs = measure_configs(args, dev, peak, peak_kind)
+        cfgs["mixed"] = {"workload": CONFIG_DESC["mixed"], "rows": rows, "block_size": case.block_size,
+                         "launches_per_step": L, "ms_per_step": round(ms, 5),
+                         "us_per_launch": round(per_launch_s * 1e6, 3),
+                         "bytes_per_launch": bytes_launch, "GBps": round(achieved, 2),
+                         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                                      "unit": "GB/s", "frac": round(achieved / peak, 4),
+                                      "peak_source": peak_kind},
+                         "what": "the headline step above"}
+        result["configs"] = cfgs
+        result["gpu_launches"] += args.steps * sum(
+            c["launches_per_step"] for k, c in cfgs.items() if k != "mixed")
 
     # Padded comparator: the same rows in a [rows][4096] slab, full width read.
     if not args.no_comparator and args.workload == "mixed":
