@@ -529,10 +529,11 @@ def run_ours(args, rank, world, pg):
     pgen = torch.Generator().manual_seed(args.seed + 4)
     pq = torch.randn(pcase.rows * pchunk, hq, hd, generator=pgen).to(torch.float16).to(dev)
     pout = torch.empty_like(pq)
+    pws = ops.alloc_prefill_workspace(pcase.rows, hq, hk, hd, pcase.block_size, device=dev)
 
     def step_prefill():
         ops.prefill(pout, pq, pd["k_pool"][0], pd["v_pool"][0], pd["block_tables"],
-                    pd["seq_lens"], pqs, pcase.scale, pcase.max_seq_len)
+                    pd["seq_lens"], pqs, pcase.scale, pcase.max_seq_len, workspace=pws)
 
     g_pf = capture(step_prefill)
     ms_pf, _ = time_graph(g_pf, args.steps, args.warmup)

@@ -148,10 +148,12 @@ int paged_kv_prefill_scatter(void* k_pool, void* v_pool, const int32_t* block_ta
  * seq_lens[r] of the calls the workspace will serve.
  *
  * The workspace must be zero-filled once after allocation.  Every decode
- * call leaves it ready for the next call (its counters back at zero), so it
+ * call that completes without PKV_DEV_ERR_TIMEOUT leaves it ready for the
+ * next call (every split-K record word it read cleared back to zero), so it
  * may be reused by later calls on the same stream, including from a CUDA
  * graph; two decode calls that run at the same time need separate
- * workspaces.
+ * workspaces.  After a call that flagged PKV_DEV_ERR_TIMEOUT, words may be
+ * left set: zero-fill the workspace again before reusing it.
  */
 size_t paged_attention_workspace_size(int rows, int q_heads, int kv_heads, int head_dim,
                                       int max_seq_len, int block_size);
@@ -267,20 +269,28 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
  * 2^31 key-tile steps in total (q_heads x 128-query tiles x 128-key tiles;
  * PKV_ERR_UNSUPPORTED beyond).
  *
- * No caller workspace: one block per SM splits the steps evenly, and a
- * 128-query tile cut between two blocks is merged through a partial result
- * kept in library-owned device memory (about 13 MB per device, allocated when
- * the library loads).  So prefill calls on one device must not overlap each
- * other: issue them on one stream, or order the streams.  Each call leaves that
- * memory ready for the next; after a PKV_DEV_ERR_TIMEOUT its arrival counters
- * may not be, and later prefill results on that device are not reliable.
+ * Workspace: one block per SM splits the steps evenly, and a 128-query tile
+ * cut between two blocks is merged through a partial result that goes
+ * through `workspace`: paged_attention_prefill_workspace_size(...) bytes of
+ * caller device memory, 256-byte aligned, zero-filled once after allocation
+ * (a smaller or misaligned one returns PKV_ERR_WORKSPACE).  Every call that
+ * completes without PKV_DEV_ERR_TIMEOUT leaves it ready for the next (its
+ * arrival words back at zero); after one that timed out, zero-fill it again.
+ * Calls on separate workspaces may overlap; calls that share one must not.
+ * workspace == NULL uses library-owned device memory instead (about 13 MB per
+ * device, held from load to exit), whose arrival words every such call clears
+ * first on `stream`: calls without a workspace on one device must not overlap
+ * each other (issue them on one stream, or order the streams).
  */
+size_t paged_attention_prefill_workspace_size(int rows, int q_heads, int kv_heads, int head_dim,
+                                              int block_size);
 int paged_attention_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* block_tables, const int32_t* seq_lens,
                             const int32_t* q_start, int rows, int total_q, int q_heads,
                             int kv_heads, int head_dim, int block_size, float scale,
                             int max_blocks_per_row, int num_blocks, int max_seq_len,
-                            int32_t* dev_err, cudaStream_t stream);
+                            void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                            cudaStream_t stream);
 
 /*
  * FP8 KV pools.  "PagedAttention" (deepconcepts.dev), section "Checking it on
@@ -434,12 +444,15 @@ int paged_attention_decode_planned(void* out, const void* q, void* k_pool, void*
  *    PKV_NOALLOC_WORKSPACE_BYTES return PKV_ERR_WORKSPACE before launch.
  *  - Set-up: the first call made on a device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current) and caches it;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The cached address
+ *    belongs to the device's context at that time: after cudaDeviceReset (or
+ *    any other teardown of that context) the cached address is stale, so a
+ *    process that resets a device must not call this entry point again.
  *  - Sharing: every call on a device uses the same array, which keeps the
  *    last call's contents.  Each call first clears the part that must start
- *    at zero (the per-row arrival counters, by cudaMemsetAsync on `stream`);
- *    the rest is written before it is read.  Calls that overlap on the GPU
- *    (for example on two streams at once) race on the array and give wrong
+ *    at zero (the split-K record words, by cudaMemsetAsync on `stream`); the
+ *    rest is written before it is read.  Calls that overlap on the GPU (for
+ *    example on two streams at once) race on the array and give wrong
  *    results: serialise them.
  */
 int paged_attention_decode_noalloc(void* out, const void* q, const void* k_pool,
@@ -448,6 +461,20 @@ int paged_attention_decode_noalloc(void* out, const void* q, const void* k_pool,
                                    int head_dim, int block_size, float scale,
                                    int max_blocks_per_row, int num_blocks, int max_seq_len,
                                    int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * pkv_debug_set_decode_hooks -- test hook for the bounded waits of the
+ * decode kernels' split-unit merge (no counterpart in the pages).  A merge
+ * polls the records of a unit's other pieces; poll_limit (0 = the default,
+ * about 2^22 polls) caps those polls, after which the merge gives up, flags
+ * PKV_DEV_ERR_TIMEOUT and its block ends.  stuck_word, if non-null, is a
+ * device word that every merge poll also waits to see non-zero: a word that
+ * nothing writes makes every merge give up.  Both apply to launches made
+ * after the call, from any thread, until changed; pass (0, NULL) to restore
+ * normal operation.  After a timed-out call, zero-fill the workspace before
+ * reusing it.  For tests of the failure path; not for production use.
+ */
+int pkv_debug_set_decode_hooks(unsigned poll_limit, const void* stuck_word);
 
 /*
  * pkv_check_error -- synchronise `stream`, copy the device error word to

@@ -20,8 +20,8 @@ namespace {
 
 constexpr size_t kScratchBytes = PKV_NOALLOC_WORKSPACE_BYTES;
 
-// Split-K partial results and per-row arrival counters of the decode kernel,
-// shared by every paged_attention_decode_noalloc call on a device.
+// Split-K records of the decode kernel, shared by every
+// paged_attention_decode_noalloc call on a device.
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -67,8 +67,9 @@ extern "C" int paged_attention_decode_noalloc(void* out, const void* q, const vo
     void* scratch = nullptr;
     const int st = scratch_for_current_device(&scratch);
     if (st != PKV_OK) return st;
-    // The array keeps the previous call's contents; the arrival counters must
-    // start at zero, the partial results are written before they are read.
+    // The array keeps the previous call's contents (words left set by a call
+    // that timed out, or by a call of another shape); the record words must
+    // start at zero.
     const size_t zero = pkv::decode_workspace_zero_bytes(rows, q_heads, kv_heads, head_dim,
                                                          max_seq_len, block_size);
     if (cudaMemsetAsync(scratch, 0, zero, stream) != cudaSuccess) return PKV_ERR_CUDA;

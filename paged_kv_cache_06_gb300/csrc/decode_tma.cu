@@ -124,6 +124,7 @@ struct Params {
     int width;      // padded comparator: columns per row (0 = paged)
     float scale_log2;
     uint32_t poll_limit;  // polls of a record batch before a merge gives up
+    const uint32_t* stuck;  // test hook: a word every merge poll also waits on (null: none)
     const unsigned char* plan;  // [grid][kPlanBytes] step plan, or null: each block makes its own
     unsigned char* records;  // unit regions of split-piece records (zero between calls)
     int32_t* dev_err;
@@ -674,6 +675,7 @@ __device__ __forceinline__ bool merge_task(const Params& p, const Task& t, int l
                     wc[b] = ld_rec(cb + j * kLLChunk);
                     all &= rec_written(wm[b]) & rec_written(wc[b]);
                 }
+                if (p.stuck) all &= *reinterpret_cast<const volatile uint32_t*>(p.stuck) != 0u;
             } while (!__all_sync(0xffffffffu, all) && ++it < p.poll_limit);
             if (it >= p.poll_limit) {
                 ok = false;
@@ -1636,6 +1638,12 @@ static int pool_map(const void* base, int64_t rows, int hk, bool fp8, CUtensorMa
                         dims, strides, box, out);
 }
 
+// Test hooks for the bounded waits of the split-unit merge (see
+// pkv_debug_set_decode_hooks); zero / null in normal use.
+static std::mutex g_hook_mutex;
+static uint32_t g_hook_poll_limit = 0;
+static const void* g_hook_stuck = nullptr;
+
 struct DeviceInfo {
     int sms = 0;
     bool attr_set[3] = {false, false, false};
@@ -1774,7 +1782,11 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     prm.limit = limit;
     prm.width = paged ? 0 : width;
     prm.scale_log2 = scale * kLog2e;
-    prm.poll_limit = kPollLimit;
+    {
+        std::lock_guard<std::mutex> lock(g_hook_mutex);
+        prm.poll_limit = g_hook_poll_limit ? g_hook_poll_limit : kPollLimit;
+        prm.stuck = static_cast<const uint32_t*>(g_hook_stuck);
+    }
     prm.plan = static_cast<const unsigned char*>(plan);
     prm.records = static_cast<unsigned char*>(workspace);
     prm.dev_err = dev_err;
@@ -1816,3 +1828,10 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
 }
 
 }  // namespace pkv
+
+extern "C" int pkv_debug_set_decode_hooks(unsigned poll_limit, const void* stuck_word) {
+    std::lock_guard<std::mutex> lock(pkv::tma::g_hook_mutex);
+    pkv::tma::g_hook_poll_limit = poll_limit;
+    pkv::tma::g_hook_stuck = stuck_word;
+    return PKV_OK;
+}

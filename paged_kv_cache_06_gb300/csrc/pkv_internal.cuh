@@ -64,11 +64,15 @@ int tiled_map_3d(const void* base, CUtensorMapDataType dtype, const int64_t dims
                  const int64_t strides[2], const int box[3], CUtensorMap* out);
 
 // The tcgen05 chunked-prefill kernel (arguments validated by the caller).
+// workspace: prefill_workspace_bytes() of caller memory (arrival words, zero
+// between calls, then partials), or null for the library-owned scratch.
+size_t prefill_workspace_bytes();
+size_t prefill_count_bytes();
 int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* block_tables, const int32_t* seq_lens,
                       const int32_t* q_start, int rows, int total_q, int q_heads, int kv_heads,
                       int block_size, float scale, int max_blocks_per_row, int num_blocks,
-                      int max_seq_len, int32_t* dev_err, cudaStream_t stream);
+                      int max_seq_len, void* workspace, int32_t* dev_err, cudaStream_t stream);
 
 int tma_decode_launch(void* out, const void* q, const void* k_base, const void* v_base,
                       const int32_t* tables, const int32_t* seq_lens, int rows, int q_heads,

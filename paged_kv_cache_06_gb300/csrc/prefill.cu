@@ -11,12 +11,21 @@
 // the row's tokens 0 .. p_r + i.
 #include "pkv_internal.cuh"
 
+extern "C" size_t paged_attention_prefill_workspace_size(int rows, int q_heads, int kv_heads,
+                                                        int head_dim, int block_size) {
+    if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads || head_dim <= 0 ||
+        block_size <= 0)
+        return 0;
+    return pkv::prefill_workspace_bytes();
+}
+
 extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_pool,
                                        const void* v_pool, const int32_t* block_tables,
                                        const int32_t* seq_lens, const int32_t* q_start, int rows,
                                        int total_q, int q_heads, int kv_heads, int head_dim,
                                        int block_size, float scale, int max_blocks_per_row,
-                                       int num_blocks, int max_seq_len, int32_t* dev_err,
+                                       int num_blocks, int max_seq_len, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_err,
                                        cudaStream_t stream) {
     using namespace pkv;
     if (rows < 0 || total_q < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads ||
@@ -31,7 +40,10 @@ extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_p
         return PKV_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID_ARG;
+    if (workspace && ((reinterpret_cast<uintptr_t>(workspace) & 255) ||
+                      workspace_bytes < prefill_workspace_bytes()))
+        return PKV_ERR_WORKSPACE;
     return prefill_tc_launch(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, rows, total_q,
                              q_heads, kv_heads, block_size, scale, max_blocks_per_row, num_blocks,
-                             max_seq_len, dev_err, stream);
+                             max_seq_len, workspace, dev_err, stream);
 }

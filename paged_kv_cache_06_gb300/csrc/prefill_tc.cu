@@ -1055,9 +1055,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace {
 
 // Partials of cut units and the merging blocks' arrival words, one slot per
-// persistent block, shared by every prefill launch on a device: launches on
-// one device run one after another (one stream, or streams the caller
-// orders), and each launch leaves the arrival words at zero.
+// persistent block, for launches made without a caller workspace; shared by
+// all such launches on a device, so those must run one after another (one
+// stream, or streams the caller orders).  Each such launch clears the arrival
+// words first.
 static __device__ __align__(256) float g_prefill_part[pkv::prefill_tc::kMaxGrid * pkv::prefill_tc::kPartFloats];
 static __device__ __align__(256) int g_prefill_count[pkv::prefill_tc::kMaxGrid * pkv::prefill_tc::kCountStride];
 
@@ -1099,11 +1100,21 @@ namespace pkv {
 
 // Launch of the tcgen05 prefill kernel; the caller has validated the
 // arguments (paged_attention_prefill).
+size_t prefill_workspace_bytes() {
+    using namespace prefill_tc;
+    return prefill_count_bytes() + (size_t)kMaxGrid * kPartFloats * sizeof(float);
+}
+
+size_t prefill_count_bytes() {
+    using namespace prefill_tc;
+    return align_up((size_t)kMaxGrid * kCountStride * sizeof(int), 256);
+}
+
 int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* v_pool,
                       const int32_t* block_tables, const int32_t* seq_lens,
                       const int32_t* q_start, int rows, int total_q, int q_heads, int kv_heads,
                       int block_size, float scale, int max_blocks_per_row, int num_blocks,
-                      int max_seq_len, int32_t* dev_err, cudaStream_t stream) {
+                      int max_seq_len, void* workspace, int32_t* dev_err, cudaStream_t stream) {
     using namespace prefill_tc;
     const int64_t pool_rows = (int64_t)num_blocks * block_size;
     int kbox = kGranule;
@@ -1152,8 +1163,19 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
     prm.vbox = vbox;
     prm.scale_log2 = scale * kLog2e;
     prm.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
-    prm.part = dv.part;
-    prm.count = dv.count;
+    const int grid = dv.sms < kMaxGrid ? dv.sms : kMaxGrid;
+    if (workspace) {
+        // caller-owned: arrival words first (zero between calls), then the partials
+        prm.count = static_cast<int*>(workspace);
+        prm.part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + prefill_count_bytes());
+    } else {
+        // library-owned: its arrival words are cleared here, so a launch that
+        // timed out leaves nothing behind for the next one
+        prm.part = dv.part;
+        prm.count = dv.count;
+        if (cudaMemsetAsync(dv.count, 0, (size_t)grid * kCountStride * sizeof(int), stream) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
     prm.dev_err = dev_err;
     static bool attr_set = false;
     if (!attr_set) {
@@ -1164,7 +1186,6 @@ int prefill_tc_launch(void* out, const void* q, const void* k_pool, const void* 
     }
     // One block per SM: every block is resident at once, so a merging block
     // never waits on a block that has not started.
-    const int grid = dv.sms < kMaxGrid ? dv.sms : kMaxGrid;
     prefill_tc_kernel<<<grid, kThreads, Smem::total(), stream>>>(km, vm, qm, prm);
     return launch_status();
 }

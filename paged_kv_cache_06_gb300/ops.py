@@ -80,8 +80,11 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_append_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I,
                                                     F, I, I, I, P, S, ctypes.c_uint, P, P]
     L.paged_attention_append_decode_fp8.restype = I
-    L.paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P]
+    L.paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, S,
+                                          P, P]
     L.paged_attention_prefill.restype = I
+    L.paged_attention_prefill_workspace_size.argtypes = [I, I, I, I, I]
+    L.paged_attention_prefill_workspace_size.restype = S
     L.paged_kv_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
     L.paged_kv_copy_blocks.restype = I
     L.paged_kv_prefill_scatter.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
@@ -93,6 +96,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.paged_attention_decode_planned.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F,
                                                  I, I, I, P, S, P, S, ctypes.c_uint, P, P]
     L.paged_attention_decode_planned.restype = I
+    L.pkv_debug_set_decode_hooks.argtypes = [ctypes.c_uint, P]
+    L.pkv_debug_set_decode_hooks.restype = I
 
 
 def status_string(status: int) -> str:
@@ -220,13 +225,28 @@ def decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
     _check("paged_attention_decode_fp8", st)
 
 
+def prefill_workspace_size(rows: int, q_heads: int, kv_heads: int, head_dim: int,
+                           block_size: int) -> int:
+    return int(lib().paged_attention_prefill_workspace_size(rows, q_heads, kv_heads, head_dim,
+                                                            block_size))
+
+
+def alloc_prefill_workspace(rows, q_heads, kv_heads, head_dim, block_size, device="cuda"):
+    """A zero-filled prefill workspace (uint8, 256-byte aligned by the allocator)."""
+    n = prefill_workspace_size(rows, q_heads, kv_heads, head_dim, block_size)
+    if n == 0:
+        raise ValueError("invalid sizes for a prefill workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def prefill(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: float,
-            max_seq_len: int, dev_err=None, stream=None):
+            max_seq_len: int, dev_err=None, stream=None, workspace=None):
     """paged_attention_prefill: causal attention of each row's chunk of new tokens.
 
-    The kernel keeps the partial results of query tiles cut between blocks
-    in library-owned device memory, so prefill calls on one device must not
-    overlap: issue them on one stream, or order the streams.
+    workspace: from alloc_prefill_workspace (calls on separate workspaces may
+    overlap), or None for library-owned memory (calls without a workspace on
+    one device must not overlap: issue them on one stream, or order the
+    streams).
     """
     for t, n, dt, nd in ((out, "out", torch.float16, 3), (q, "q", torch.float16, 3),
                          (k_pool, "k_pool", torch.float16, 4), (v_pool, "v_pool", torch.float16, 4),
@@ -234,6 +254,8 @@ def prefill(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: floa
                          (seq_lens, "seq_lens", torch.int32, 1), (q_start, "q_start", torch.int32, 1)):
         _need(t, n, dt, nd)
     _need_err(dev_err)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1)
     total, hq, d = q.shape
     nb, bs, hk, _ = k_pool.shape
     rows = seq_lens.shape[0]
@@ -242,7 +264,8 @@ def prefill(out, q, k_pool, v_pool, block_tables, seq_lens, q_start, scale: floa
     st = lib().paged_attention_prefill(
         _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
         _ptr(q_start), rows, total, hq, hk, d, bs, float(scale), block_tables.shape[1], nb,
-        int(max_seq_len), _ptr(dev_err), _stream(stream))
+        int(max_seq_len), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _ptr(dev_err), _stream(stream))
     _check("paged_attention_prefill", st)
 
 
@@ -444,3 +467,14 @@ def check_error(dev_err: torch.Tensor, stream=None) -> int:
     st = lib().pkv_check_error(_ptr(dev_err), _stream(stream), ctypes.byref(host))
     _check("pkv_check_error", st)
     return int(host.value)
+
+
+def debug_set_decode_hooks(poll_limit: int = 0, stuck_word: Optional[torch.Tensor] = None) -> None:
+    """pkv_debug_set_decode_hooks: cap the merge's polls and/or make every
+    merge also wait on a device word (a word that nothing writes makes each
+    merge give up and flag PKV_DEV_ERR_TIMEOUT).  (0, None) restores normal
+    operation.  Test hook."""
+    if stuck_word is not None:
+        _need(stuck_word, "stuck_word", torch.int32, 1)
+    _check("pkv_debug_set_decode_hooks",
+           lib().pkv_debug_set_decode_hooks(int(poll_limit), _ptr(stuck_word)))

@@ -203,20 +203,76 @@ def test_padded_comparator_matches_oracle(cuda_device):
     assert np.allclose(cont, ref, rtol=1e-12, atol=1e-12)
 
 
-# --- full-size workloads (sampled rows checked against the oracle) ---------------
+# --- full-size workloads, every row, in the launch the benchmark times ----------
+
+def run_fused(case, layer=0, pdl=True):
+    """One layer through paged_attention_append_decode with programmatic
+    dependent launch, as the benchmark launches it (rows with a negative
+    position append nothing)."""
+    d = wl.to_device(case)
+    kp, vp = d["k_pool"][layer], d["v_pool"][layer]
+    ws = ops.alloc_workspace(case.rows, case.q_heads, case.kv_heads, case.head_dim,
+                             case.max_seq_len, case.block_size)
+    out = torch.full((case.rows, case.q_heads, case.head_dim), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    ops.append_decode(out, d["q"][layer], kp, vp, d["block_tables"], d["seq_lens"],
+                      d["positions"], d["k_new"][layer], d["v_new"][layer], case.scale,
+                      case.max_seq_len, ws, pdl=pdl)
+    torch.cuda.synchronize()
+    return out, kp, vp
+
 
 @pytest.mark.parametrize("name", ["uniform", "mixed", "shared", "long"])
-def test_full_size_workloads_sampled(cuda_device, name):
+def test_full_size_workloads_every_row(cuda_device, name):
     if name in ("uniform", "mixed"):
         case = wl.WORKLOADS[name](layers=1)
     else:
         case = wl.WORKLOADS[name]()
-    out, *_ = run_gpu(case)
-    L = case.seq_lens
-    rows = sorted({int(np.argmax(L)), int(np.argmin(L)), 0, case.rows - 1, case.rows // 2})
-    _, _, ref = oracle_after_append(case, 0, rows=rows)
-    assert_close(out[rows], ref, name)
-    assert torch.isfinite(out.float()).all()
+    out, kp, vp = run_fused(case)
+    ek, ev, ref = oracle_after_append(case, 0)
+    assert np.array_equal(bits(kp), ek) and np.array_equal(bits(vp), ev), f"{name}: pools"
+    assert_close(out, ref, name)
+
+
+def test_mixed_28_layer_pdl_graph_every_row(cuda_device):
+    # Exactly the benchmark's step: 28 fused launches with programmatic
+    # dependent launch, captured in one CUDA graph and replayed.
+    case = wl.mixed(layers=28)
+    d = wl.to_device(case)
+    ws = ops.alloc_workspace(case.rows, 12, 2, 128, case.max_seq_len, 64)
+    outs = torch.zeros(case.layers, case.rows, 12, 128, dtype=torch.float16, device="cuda")
+    k0 = [d["k_pool"][l].clone() for l in range(case.layers)]
+    v0 = [d["v_pool"][l].clone() for l in range(case.layers)]
+
+    def step(pdl):
+        for l in range(case.layers):
+            ops.append_decode(outs[l], d["q"][l], d["k_pool"][l], d["v_pool"][l],
+                              d["block_tables"], d["seq_lens"], d["positions"], d["k_new"][l],
+                              d["v_new"][l], case.scale, case.max_seq_len, ws, pdl=pdl)
+
+    step(False)
+    torch.cuda.synchronize()
+    eager = outs.clone()
+    for l in range(case.layers):  # the pools as they were before the step
+        d["k_pool"][l].copy_(k0[l])
+        d["v_pool"][l].copy_(v0[l])
+    outs.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(True)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), outs.view(torch.int16))
+    for layer in (case.layers // 2, case.layers - 1):
+        ek, ev, ref = oracle_after_append(case, layer)
+        assert np.array_equal(bits(d["k_pool"][layer]), ek), f"layer {layer} k pool"
+        assert np.array_equal(bits(d["v_pool"][layer]), ev), f"layer {layer} v pool"
+        assert_close(outs[layer], ref, f"pdl graph layer {layer}")
 
 
 # --- device-side error reporting (never a fault) -----------------------------------

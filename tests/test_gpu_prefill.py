@@ -35,15 +35,20 @@ def prefill_case(lengths, chunks, bs, seed):
     return case, q, qs
 
 
-def run(case, q, qs, dev_err=None, tables=None):
+def run(case, q, qs, dev_err=None, tables=None, workspace=None, stream=None, sync=True):
     d = wl.to_device(case)
     bt = d["block_tables"] if tables is None else torch.from_numpy(tables).cuda()
     gq = torch.from_numpy(q.view(np.int16)).view(torch.float16).cuda()
     out = torch.full(gq.shape, float("nan"), dtype=torch.float16, device="cuda")
-    ops.prefill(out, gq, d["k_pool"][0], d["v_pool"][0], bt, d["seq_lens"],
-                torch.from_numpy(qs).cuda(), case.scale, case.max_seq_len, dev_err=dev_err)
-    torch.cuda.synchronize()
-    return out
+    qst = torch.from_numpy(qs).cuda()
+    if stream is not None:
+        stream.wait_stream(torch.cuda.current_stream())
+    ops.prefill(out, gq, d["k_pool"][0], d["v_pool"][0], bt, d["seq_lens"], qst, case.scale,
+                case.max_seq_len, dev_err=dev_err, workspace=workspace, stream=stream)
+    if sync:
+        torch.cuda.synchronize()
+        return out
+    return out, (d, gq, qst, bt)  # keep the inputs alive until the caller synchronises
 
 
 @pytest.mark.parametrize("lengths,chunks,bs", [
@@ -78,6 +83,46 @@ def test_prefill_512_chunks_on_4096_rows_sampled(cuda_device):
     ref_all = oracle.paged_prefill(q, case.k_pool[0], case.v_pool[0], case.block_tables,
                                    case.seq_lens, qs, case.scale, num_threads=oracle.default_threads())
     assert_close(out[torch.from_numpy(idx)], ref_all[idx], "512-token chunks")
+
+
+def test_prefill_benchmark_launch_every_query(cuda_device):
+    # The benchmark's prefill launch: 8 rows whose newest 512 tokens are the
+    # chunk, at 4096 tokens of context, 64-token blocks, seeds as there;
+    # every query of every row against the oracle.
+    case = wl.custom([4096] * 8, 64, seed=3, layers=1, append=False, nan_fill=False)
+    chunk = 512
+    qs = np.arange(0, chunk * (case.rows + 1), chunk, dtype=np.int32)
+    gen = torch.Generator().manual_seed(4)
+    q = torch.randn(case.rows * chunk, case.q_heads, case.head_dim, generator=gen).to(torch.float16)
+    qbits = q.view(torch.int16).numpy().view(np.uint16)
+    out = run(case, qbits, qs)
+    ref = oracle.paged_prefill(qbits, case.k_pool[0], case.v_pool[0], case.block_tables,
+                               case.seq_lens, qs, case.scale, num_threads=oracle.default_threads())
+    assert_close(out, ref, "benchmark prefill launch")
+
+
+def test_prefill_calls_on_separate_workspaces_overlap(cuda_device):
+    # Two prefill calls, each with its own caller workspace, enqueued on two
+    # streams at once (neither waits for the other): both match the oracle.
+    # Then the same two back to back on one stream through the library-owned
+    # scratch (no workspace).
+    c1, q1, qs1 = prefill_case([3000, 20, 2500], [700, 20, 300], 16, seed=31)
+    c2, q2, qs2 = prefill_case([8192], [128], 64, seed=32)
+    ws1 = ops.alloc_prefill_workspace(c1.rows, c1.q_heads, c1.kv_heads, c1.head_dim, c1.block_size)
+    ws2 = ops.alloc_prefill_workspace(c2.rows, c2.q_heads, c2.kv_heads, c2.head_dim, c2.block_size)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o1, keep1 = run(c1, q1, qs1, workspace=ws1, stream=s1, sync=False)
+    o2, keep2 = run(c2, q2, qs2, workspace=ws2, stream=s2, sync=False)
+    torch.cuda.synchronize()
+    refs = []
+    for c, q, qs, o in ((c1, q1, qs1, o1), (c2, q2, qs2, o2)):
+        ref = oracle.paged_prefill(q, c.k_pool[0], c.v_pool[0], c.block_tables, c.seq_lens, qs,
+                                   c.scale, num_threads=oracle.default_threads())
+        assert_close(o, ref, "overlapping call")
+        refs.append(ref)
+    del keep1, keep2
+    for c, q, qs, ref in ((c1, q1, qs1, refs[0]), (c2, q2, qs2, refs[1])):
+        assert_close(run(c, q, qs), ref, "library-owned scratch")
 
 
 def test_prefill_bit_identical_under_block_permutation(cuda_device):

@@ -398,6 +398,43 @@ def test_fp8_quantize_divides_in_binary32_first():
     assert np.array_equal(oracle.fp8_quantize(x, s), expect)
 
 
+def test_fp8_quantize_matches_torch_on_many_draws_and_near_ties():
+    # The quotient x / s is formed in binary32 and then rounded to E4M3
+    # (nearest, ties to even).  PyTorch does the same independently:
+    # (x.float() / s).to(float8_e4m3fn).  Compared on 2e5 fp16 draws over many
+    # binades and on fp16 values whose quotient lies within a few binary32
+    # ulps of an E4M3 rounding tie, where a quotient formed in double
+    # precision (or rounded twice) would pick the other neighbour.  Only
+    # quotients inside the E4M3 range are compared: beyond it the oracle
+    # saturates and PyTorch's conversion does not.
+    torch = pytest.importorskip("torch")
+    g = torch.Generator().manual_seed(11)
+    xs = []
+    for _ in range(4):
+        e = torch.randint(-14, 16, (50000,), generator=g).float()
+        xs.append((torch.randn(50000, generator=g) * torch.exp2(e)).to(torch.float16))
+    # near ties: midpoints between neighbouring positive E4M3 values, times s,
+    # rounded to fp16, and the fp16 values one and two steps either side
+    codes = np.arange(0x01, 0x7E, dtype=np.uint8)
+    vals = oracle.fp8_e4m3_to_double(codes)
+    mids = (vals[:-1] + vals[1:]) / 2
+    for s in (np.float32(0.37), np.float32(0.0123), np.float32(1.0), np.float32(3.3)):
+        base = torch.from_numpy(mids * float(s)).to(torch.float16)
+        near = [base]
+        bits16 = base.view(torch.int16)
+        for k in (-2, -1, 1, 2):
+            near.append((bits16 + k).view(torch.float16))
+        near = torch.cat(near)
+        near = torch.cat([near, -near])
+        for x in xs + [near]:
+            q = x.float() / torch.tensor(s)
+            keep = torch.isfinite(q) & (q.abs() <= 448)
+            x = x[keep]
+            ref = (x.float() / torch.tensor(s)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            ours = oracle.fp8_quantize(x.view(torch.int16).numpy().view(np.float16), s)
+            assert np.array_equal(ours, ref), f"scale {s}: {int((ours != ref).sum())} of {ref.size} differ"
+
+
 def test_fp8_append_writes_quantised_slots_only():
     rng = np.random.default_rng(4)
     nb, bs, hk, d, rows = 6, 16, 2, 8, 3

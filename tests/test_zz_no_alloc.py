@@ -5,9 +5,11 @@ host framework that owns all device memory through its own pool, or a serving
 loop that forbids cudaMalloc after start-up because it can synchronise the
 device.  For them the library keeps its split-K scratch in one static device
 array.  These checks call that entry point through the C ABI and compare it
-with the workspace-taking entry point, within the same tolerance as the other
-GPU tests, on two calls in a row (the array keeps the previous call's
-contents, so the second call checks that the entry point re-arms it).
+with the workspace-taking entry point on two calls in a row (the array keeps
+the previous call's contents, so the second call checks that the entry point
+re-arms it).  Both run the same kernel on the same work split, so the outputs
+must be bit-identical; the calls must also leave the device's free memory
+unchanged.
 
 The file name sorts last so a run that stops at the first failure has already
 run every other test; it also passes when run alone in a fresh process.
@@ -32,6 +34,8 @@ def _close(a: torch.Tensor, b: torch.Tensor):
     y = b.float().cpu().numpy()
     assert np.all(np.isfinite(x))
     assert np.all(np.abs(x - y) <= ATOL + RTOL * np.abs(y))
+    # the same kernel on the same split: bit for bit
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def _reference_and_inputs(case):
@@ -52,11 +56,20 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(cuda_device
     case = wl.mixed(layers=1)
     assert ops.workspace_size(case.rows, 12, 2, 128, case.max_seq_len, 64) <= NOALLOC_BYTES
     d, kp, vp, ref = _reference_and_inputs(case)
-    for _ in range(2):
-        out = torch.full_like(ref, float("nan"))
+    outs = [torch.full_like(ref, float("nan")) for _ in range(3)]
+    # the first call may set up the array's address on this device
+    ops.decode_noalloc(outs[0], d["q"][0], kp, vp, d["block_tables"], d["seq_lens"], case.scale,
+                       case.max_seq_len)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for out in outs[1:]:
         ops.decode_noalloc(out, d["q"][0], kp, vp, d["block_tables"], d["seq_lens"], case.scale,
                            case.max_seq_len)
         torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+    for out in outs:
         _close(out, ref)
 
 
