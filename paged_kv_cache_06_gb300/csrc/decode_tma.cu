@@ -1378,7 +1378,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + Smem::bars;
     const uint32_t bar_empty = bar_full + kStages * 8;
-    const uint32_t bar_slot = bar_full + 2 * kStages * 8;
     BlockPlan* bp = reinterpret_cast<BlockPlan*>(smem + Smem::plan);
     volatile int* sm_flags = reinterpret_cast<volatile int*>(smem + Smem::flags);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
@@ -1400,24 +1399,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     // grid to complete before touching anything this grid writes.
     griddep_launch();
     if (warp == kConsumerWarps) {
-        if (lane == 0) {
-            // fetch the tensor-map descriptors now; the first copy would wait for them
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
-        }
         // the step's plan for this block: one 16-byte load per lane
         if (prm.plan)
             reinterpret_cast<uint4*>(bp)[lane] =
                 __ldg(reinterpret_cast<const uint4*>(prm.plan + (size_t)cta * kPlanBytes) + lane);
     }
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kStreamWarps);
-        }
-#pragma unroll 1
-        for (int s = 0; s < kRing; ++s) mbar_init(bar_slot + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sm_flags[0] = 0;  // abort
         sm_flags[4] = sm_flags[5] = 0;  // a merge task's poll gave up
     }
@@ -1443,7 +1430,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
     }
     const int mode = bp->mode;
-    const int g0 = bp->g0, g1 = bp->g1;
+    const int g0 = bp->g0;
+    if (mode == kModeStream) {
+        // only stream mode uses the stage barriers and the tiled copies
+        if (tid == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(bar_full + 8 * s, 1);
+                mbar_init(bar_empty + 8 * s, kStreamWarps);
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            // fetch the tensor-map descriptors now; the first copy would wait for them
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+        }
+        __syncthreads();
+    }
     Ctx cx;
     cx.smem = smem;
     cx.sbase = sbase;
