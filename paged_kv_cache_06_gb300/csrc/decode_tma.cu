@@ -19,23 +19,24 @@
 // all the layers of the step.  The part of a unit inside one block is a
 // piece.
 //
-// Block layout.  Warps 0-6 consume, warp 7 produces, in one of two modes:
+// Block layout.  Warps 0-6 consume; warp 7 does the block's row work (the
+// fused append) after the dependency wait.  Two modes, chosen per block:
 //   * burst: the block's whole range fits the ring of twelve 8 KB granule
 //     slots and covers at most four pieces.  The seven consumer warps are
 //     dealt to pieces in proportion to their size; before the dependency
-//     wait each stages its own granules with 16-byte cp.async copies (rows
-//     past the length zero-filled), each then attends to its granules, and
-//     the warps of a piece combine their states.  Warp 7 only does the
-//     block's row work (the fused append).  Plain asynchronous copies are
-//     used here because, in a grid launched with programmatic stream
-//     serialization, tiled bulk copies issued before the dependency wait
-//     complete only after the preceding grid has completed, while plain
-//     loads and cp.async proceed at once.
-//   * stream: the producer resolves each granule's physical block from the
-//     table and issues TMA tiled copies (a 16-token x 64-dim box, 128-byte
-//     swizzle, never crossing a physical block) into the ring as three
-//     stages of four granules, one granule per warp (warps 0-3) per stage,
-//     and warp 0 absorbs the others' states as each piece ends.
+//     wait each stages its own granules, each then attends to its granules,
+//     and the warps of a piece combine their states.
+//   * stream: warps 0-3 each stream an equal contiguous share of the range
+//     through three slots of their own, two granules' copies in flight; a
+//     unit wholly inside one share is finished by its warp, the others are
+//     combined by the warps holding their states once every share is done.
+// Granules are staged with 16-byte cp.async copies (rows past the length
+// zero-filled) in the 128-byte-swizzled layout of a tiled copy.  Plain
+// asynchronous copies are used because, in a grid launched with programmatic
+// stream serialization, tiled bulk copies issued before the dependency wait
+// complete only after the preceding grid has completed, while cp.async
+// proceeds at once; and because a single thread's tiled copies issue at a
+// lower rate than a warp's cp.async.
 // Per granule (16 tokens) and group of query heads (up to 8):
 //   S^T[16 tok][8 heads] = K[16 tok][128] . Q^T        (mma.sync m16n8k16)
 //   online softmax per head in fp32, base-2 exponent
@@ -77,16 +78,12 @@ namespace pkv {
 namespace tma {
 
 constexpr int kGranule = 16;        // tokens per box and per consumer warp step
-constexpr int kTileGranules = 4;    // stream mode: granules per stage (one per stream warp)
-constexpr int kStages = 3;
-constexpr int kRing = kStages * kTileGranules;  // granule slots
+constexpr int kRing = 12;           // granule slots
 constexpr int kConsumerWarps = 7;   // burst mode
-constexpr int kStreamWarps = 4;     // stream mode: warps 0-3 consume, 4-6 leave
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kMaxCtas = 1024;
 constexpr int kMaxRows = 1024;
-constexpr int kMaxPieces = 32; // append positions prefetched for a block's first pieces
 constexpr int kBurstPieces = 4;
 constexpr int kMaxTasks = 2;   // split pieces of a block: its first and its last
 constexpr int kMergeWays = 8;  // most participants of a split unit's merge
@@ -102,7 +99,6 @@ constexpr int kModeIdle = 0, kModeBurst = 1, kModeStream = 2;
 constexpr uint32_t kPlanBytes = 512;             // one block's plan
 constexpr int kPlanThreads = 1024;               // threads of the plan kernel
 constexpr int kFp8MaxKvHeads = 16;                // FP8 pools: per-head scales kept in shared memory
-constexpr uint32_t kQBytes = 8 * 256;            // up to 8 query heads x 128 dims
 constexpr float kLog2e = 1.4426950408889634f;
 
 // named barriers (0 is __syncthreads)
@@ -174,15 +170,11 @@ static_assert(kConsumerWarps <= 8, "warp shares fit the plan");
 // Shared memory carve-up (offsets from a 1024-aligned base).
 struct Smem {
     static constexpr uint32_t ring = 0;
-    static constexpr uint32_t q = ring + kRing * kSlotBytes;                        // [stages] stream queries
-    static constexpr uint32_t bars = q + kStages * kQBytes;                         // full[S], empty[S], slot[R]
-    static constexpr uint32_t desc = bars + (2 * kStages + kRing) * 8;             // TileDesc[S]
-    static constexpr uint32_t plan = desc + kStages * 64;                           // BlockPlan
+    static constexpr uint32_t sinfo = ring + kRing * kSlotBytes;                    // stream: unit of each slot [kRing]
+    static constexpr uint32_t plan = sinfo + kRing * 4;                             // BlockPlan (16-byte aligned)
     static constexpr uint32_t flags = plan + kPlanBytes;                            // misc ints
     static constexpr uint32_t scales = flags + 16 * 4;                              // FP8: k, v scale [2][16]
-    static constexpr uint32_t ppos = scales + 2 * kFp8MaxKvHeads * 4;               // piece positions [32]
-    static constexpr uint32_t prm = ppos + kMaxPieces * 4;                          // copy of the launch's Params
-    static constexpr uint32_t part = prm + 256;                                     // scan partials [kThreads]
+    static constexpr uint32_t part = scales + 2 * kFp8MaxKvHeads * 4;               // scan partials [kThreads]
     static constexpr uint32_t prefix = part + kThreads * 4;                         // rows + 1 ints
     __host__ __device__ static constexpr uint32_t lens(int rows) { return prefix + (uint32_t)(rows + 1) * 4; }
     __host__ __device__ static constexpr uint32_t total(int rows) { return lens(rows) + (uint32_t)rows * 4 + 1024; }
@@ -204,21 +196,6 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-
-// Stream-mode tile descriptor: written by the producer before the stage's
-// full barrier is armed, read by the consumers after it completes.
-struct TileDesc {
-    int ustart;                 // unit's first granule (global index)
-    int pend;                   // end of this block's piece of the unit (global, exclusive)
-    int flags;                  // kFirst | kLast | kEnd
-    int r, kvh, ng;             // unit (row, KV head), granules in this tile
-    int tok0;                   // unit-local token index of the tile's first granule
-    int n;                      // unit's granule count
-    int valid[kTileGranules];   // valid tokens per granule (0 = skipped block)
-    int pad[4];
-};
-static_assert(sizeof(TileDesc) == 64, "descriptor size");
-constexpr int kFirst = 1, kLast = 2, kEnd = 4, kBlockLast = 8;
 
 __device__ __forceinline__ int granules_of(int L) { return (L + kGranule - 1) / kGranule; }
 
@@ -373,6 +350,27 @@ __device__ __forceinline__ bool prepare_granule(unsigned char* slot_ptr, int val
     return wrote;
 }
 
+// The copies of stage_granule, from the byte offset `row0` of the granule's
+// first token (for its KV head) in both pools, rows `rstride` bytes apart.
+template <bool kFp8>
+__device__ __forceinline__ void stage_rows(uint32_t slot, const unsigned char* kpool,
+                                           const unsigned char* vpool, int64_t row0, uint32_t rstride,
+                                           int valid, int lane) {
+    const int c = lane & 7, r0 = lane >> 3;  // chunk; first of the rows r0, r0 + 4, ...
+    const unsigned char* kb = kpool + row0 + c * 16;
+    const unsigned char* vb = vpool + row0 + c * 16;
+#pragma unroll
+    for (int k = 0; k < (kFp8 ? 8 : 16); ++k) {
+        const int r = r0 + 4 * (k & 3), b = k >> 2;  // row, box
+        const unsigned char* src = ((kFp8 ? b : b >> 1) ? vb : kb) + (r < valid ? r : 0) * rstride +
+                                   (kFp8 ? 0 : (b & 1) * 128);
+        const uint32_t dst = slot + b * kBoxBytes + r * 128 + ((c ^ (r & 7)) << 4);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                     "r"(r < valid ? 16 : 0)
+                     : "memory");
+    }
+}
+
 // Stages one granule into `slot` (shared address) with 16-byte cp.async
 // copies by one warp, in the layout the tiled copies produce: fp16 pools as
 // four boxes (K dims 0-63, K 64-127, V 0-63, V 64-127) of 16 rows x 128 B,
@@ -387,21 +385,9 @@ __device__ __forceinline__ void stage_granule(uint32_t slot, const unsigned char
                                               const unsigned char* vpool, int64_t zrow, int hk,
                                               int kvh, int valid, int lane) {
     constexpr int kRowBytes = kFp8 ? 128 : 256;  // one token of one KV head
-    const int64_t row0 = (zrow * hk + kvh) * kRowBytes;
-    const uint32_t rstride = (uint32_t)hk * kRowBytes;
-    const int c = lane & 7, r0 = lane >> 3;  // chunk; first of the rows r0, r0 + 4, ...
-#pragma unroll
-    for (int k = 0; k < (kFp8 ? 8 : 16); ++k) {
-        const int r = r0 + 4 * (k & 3), b = k >> 2;  // row, box
-        const unsigned char* src = ((kFp8 ? b : b >> 1) ? vpool : kpool) + row0 +
-                                   (r < valid ? r : 0) * rstride + (kFp8 ? 0 : (b & 1) * 128) + c * 16;
-        const uint32_t dst = slot + b * kBoxBytes + r * 128 + ((c ^ (r & 7)) << 4);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                     "r"(r < valid ? 16 : 0)
-                     : "memory");
-    }
+    stage_rows<kFp8>(slot, kpool, vpool, (zrow * hk + kvh) * kRowBytes, (uint32_t)hk * kRowBytes, valid,
+                     lane);
 }
-
 // FP8 pools: the producer lands a granule's E4M3 K box (16 tokens x 128
 // bytes, 128-byte swizzle) at +0 and its V box at +2 KB of the slot; the
 // owning warp widens both in place to the fp16 slot layout attend expects
@@ -560,18 +546,17 @@ __device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, 
 }
 
 // Warp j of a piece's k warps (k <= kConsumerWarps), whose states are dumped
-// in ring slots (state s in slot wa[s] - base, or base + s when wa is null):
-// combines them through their log-sum-exp for chunks c = j, j + k, ... and
-// emits those; warp 0 also emits the m/l.  Every state's offset, maximum and
-// sum is loaded up front, the weights are computed once, and each chunk's k
-// loads are issued together, so the chains overlap.
-__device__ void combine_dumps(const PieceOut& po, const unsigned char* ring, const int* wa, int base,
-                              int k, int j, int lane) {
+// in ring slots slot[0 .. k-1]: combines them through their log-sum-exp for
+// chunks c = j, j + k, ... and emits those; warp 0 also emits the m/l.  Every
+// state's offset, maximum and sum is loaded up front, the weights are
+// computed once, and each chunk's k loads are issued together, so the chains
+// overlap.
+__device__ void combine_dumps(const PieceOut& po, const unsigned char* ring,
+                              const int (&slot)[kConsumerWarps], int k, int j, int lane) {
     const int tq = lane & 3;
     uint32_t off[kConsumerWarps];
 #pragma unroll
-    for (int s = 0; s < kConsumerWarps; ++s)
-        off[s] = s < k ? (uint32_t)((wa ? wa[s] - base : base + s)) * kSlotBytes : 0u;
+    for (int s = 0; s < kConsumerWarps; ++s) off[s] = (uint32_t)slot[s < k ? s : 0] * kSlotBytes;
     float4 ml[kConsumerWarps];
 #pragma unroll
     for (int s = 0; s < kConsumerWarps; ++s)
@@ -591,6 +576,7 @@ __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring, con
         L0 += ml[s].x * ml[s].z;
         L1 += ml[s].y * ml[s].w;
     }
+#pragma unroll 1
     for (int c = j; c < 8; c += k) {
         float4 v[kConsumerWarps];
 #pragma unroll
@@ -992,334 +978,290 @@ __device__ void row_work(const Params& p, int cta, int G, int lane) {
 // functions.
 struct Ctx {
     unsigned char* smem;
-    uint32_t sbase, bar_full, bar_empty;
+    uint32_t sbase;
     BlockPlan* bp;
     volatile int* flags;
-    TileDesc* desc;
     int* pre;   // granule prefix over rows
     int* len;   // clamped lengths
-    int* ppos;  // append positions of the block's first pieces
     const float* ks;  // FP8 scales (shared memory)
     const float* vs;
     int W, Geff;
 };
 
-// Stream mode, producer warp: walks the block's range in tiles of up to four
-// granules of one unit, three stages deep, then does the block's row work and
-// drains its copies.
-template <bool kPaged, bool kFp8>
-__device__ __noinline__ void stream_produce(const CUtensorMap* kmap, const CUtensorMap* vmap,
-                                            const Params& p, const Ctx& cx, int cta, int lane) {
-    constexpr uint32_t kGranuleLoad = kFp8 ? 2 * kBoxBytes : kSlotBytes;
-    const BlockPlan* bp = cx.bp;
-    const int g0 = bp->g0, g1 = bp->g1, rows = p.rows, hk = p.hk, G = gridDim.x;
-    const int* sm_pre = cx.pre;
-    const int* sm_len = cx.len;
-    TileDesc* sm_desc = cx.desc;
-    const uint32_t sbase = cx.sbase, bar_full = cx.bar_full, bar_empty = cx.bar_empty;
-    int tile = 0;
-    bool waited = false;
-    bool aborted = false;
-    const uint32_t qbytes = (uint32_t)p.group * 256u;
-    // Stages armed before the dependency wait get their query copies
-    // after it (the query may be written by the preceding kernel).
-    auto wait_and_flush = [&]() {
-        if (waited) return;
-        griddep_wait();
-        waited = true;
-        if (lane == 0)
-            for (int t = 0; t < tile && t < kStages; ++t) {
-                const TileDesc* d = sm_desc + t;
-                if (d->flags & kFirst)
-                    bulk_load(sbase + Smem::q + t * kQBytes,
-                              p.q + ((int64_t)d->r * p.hq + d->kvh * p.group) * kHeadDim, qbytes,
-                              bar_full + 8 * t);
-            }
-    };
-    for (int bg = g0; bg < g1 && !aborted; bg += 32) {
-        const int nbat = min(32, g1 - bg);
-        // Lane j resolves granule bg + j: unit, valid tokens, physical row.
-        int u = -1, r = 0, kvh = 0, n = 1, ustart = 0, tok = 0, valid = 0, zrow = 0;
-        bool issue = false;
-        if (lane < nbat) {
-            const int gg = bg + lane;
-            int lo = 0, hi = rows - 1;
-            while (lo < hi) {  // largest row with sm_pre[row] <= gg
-                const int mid = (lo + hi + 1) >> 1;
-                if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
-            }
-            r = lo;
-            n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-            kvh = (gg - sm_pre[r]) / n;
-            ustart = sm_pre[r] + kvh * n;
-            u = r * hk + kvh;
-            tok = (gg - ustart) * kGranule;
-            valid = min(kGranule, sm_len[r] - tok);
-            if (valid < 0) valid = 0;
-            if (kPaged) {
-                const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
-                if (pb < 0 || pb >= p.nb) {
-                    flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-                    valid = 0;
-                } else {
-                    zrow = pb * p.bs + tok % p.bs;
-                    issue = true;
-                }
-            } else {
-                zrow = r * p.width + tok;
-                issue = true;
-            }
-        }
-        int j = 0;
-        while (j < nbat) {
-            // A tile: up to 4 consecutive granules of one unit.
-            const int uj = __shfl_sync(0xffffffffu, u, j);
-            const unsigned same = __ballot_sync(0xffffffffu, lane < nbat && u == uj) >> j;
-            const unsigned gap = ~same;
-            int ng = gap == 0 ? 32 : __ffs(gap) - 1;
-            ng = min(min(ng, kTileGranules), nbat - j);
-            const int r_j = __shfl_sync(0xffffffffu, r, j);
-            const int kvh_j = __shfl_sync(0xffffffffu, kvh, j);
-            const int n_j = __shfl_sync(0xffffffffu, n, j);
-            const int us_j = __shfl_sync(0xffffffffu, ustart, j);
-            const int tok_j = __shfl_sync(0xffffffffu, tok, j);
-            const int gstart = bg + j;
-            const int pend = min(g1, us_j + n_j);
-            const int pstart = max(g0, us_j);
-            const bool first = gstart == pstart;
-            const bool last = gstart + ng == pend;
-            if (!waited && tile >= kStages) wait_and_flush();
-            const int s = tile % kStages;
-            const uint32_t round = (uint32_t)tile / kStages;
-            if (!mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
-                if (lane == 0) {
-                    cx.flags[0] = 1;
-                    flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-                }
-                aborted = true;
-                break;
-            }
-            const bool mine = lane >= j && lane < j + ng;
-            TileDesc* d = sm_desc + s;
-            if (lane == 0) {
-                d->ustart = us_j;
-                d->pend = pend;
-                d->flags = (first ? kFirst : 0) | (last ? kLast : 0) |
-                           (last && pend == g1 ? kBlockLast : 0);
-                d->r = r_j;
-                d->kvh = kvh_j;
-                d->ng = ng;
-                d->tok0 = tok_j;
-                d->n = n_j;
-            }
-            if (lane < kTileGranules && lane >= ng) d->valid[lane] = 0;
-            if (mine) d->valid[lane - j] = valid;
-            const uint32_t nissue = __popc(__ballot_sync(0xffffffffu, mine && issue));
-            __syncwarp();
-            const uint32_t fb = bar_full + 8 * s;
-            if (lane == 0) mbar_arrive_expect_tx(fb, nissue * kGranuleLoad + (first ? qbytes : 0u));
-            __syncwarp();
-            if (mine && issue) {
-                const uint32_t dst = sbase + Smem::ring + (s * kTileGranules + lane - j) * kSlotBytes;
-                if (kFp8) {
-                    tma_load_3d(dst, kmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kBoxBytes, vmap, 0, kvh, zrow, fb);
-                } else {
-                    tma_load_3d(dst, kmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kBoxBytes, kmap, 64, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV, vmap, 0, kvh, zrow, fb);
-                    tma_load_3d(dst + kSlotV + kBoxBytes, vmap, 64, kvh, zrow, fb);
-                }
-            }
-            if (first && lane == 0 && waited)
-                bulk_load(sbase + Smem::q + s * kQBytes,
-                          p.q + ((int64_t)r_j * p.hq + kvh_j * p.group) * kHeadDim, qbytes, fb);
-            ++tile;
-            j += ng;
-        }
-    }
-    wait_and_flush();
-    if (!aborted) {
-        // End marker: an empty stage whose descriptor says "no more tiles".
-        const int s = tile % kStages;
-        const uint32_t round = (uint32_t)tile / kStages;
-        if (mbar_wait(bar_empty + 8 * s, (round & 1) ^ 1)) {
-            if (lane == 0) {
-                sm_desc[s].flags = kEnd;
-                mbar_arrive(bar_full + 8 * s);
-            }
-            ++tile;
-        } else if (lane == 0) {
-            cx.flags[0] = 1;
-            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-        }
-    }
-    if (kPaged) row_work<kFp8>(p, cta, G, lane);
-    // Drain: the copies of every armed stage land before the block exits.
-    for (int t = tile - kStages; t < tile; ++t) {
-        if (t < 0) continue;
-        if (!mbar_wait(bar_full + 8 * (t % kStages), (uint32_t)(t / kStages) & 1) && lane == 0)
-            flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-    }
+// Stream mode: warps 0 .. kSWarps-1 each stream an equal contiguous share
+// [wa, wb) of the block's range through their own kSSlots ring slots, with
+// kSSlots - 1 granules' copies in flight (16-byte cp.async; the first ones go
+// out before the dependency wait).  A unit that lies wholly in one warp's
+// share is finished by that warp (fp16 output straight from registers).  A
+// unit that a warp shares with other warps or blocks leaves a state: at the
+// warp's end in its slot 0, or, when it is the warp's first unit and ends
+// before the warp's share does, in the warp's global scratch slot (reloaded
+// into its slot 1 at the end).  After a barrier of the stream warps each such
+// unit is combined by the warps that hold its states and emitted (fp16
+// output, or the block's record of a split unit), as in burst mode.
+constexpr int kSWarps = 4;                 // stream warps
+constexpr int kSSlots = kRing / kSWarps;   // ring slots per stream warp
+constexpr int kSDepth = kSSlots - 1;       // copies in flight ahead of the granule consumed
+static_assert(kSSlots >= 2 && kSWarps * kSSlots == kRing, "stream slots");
+static_assert(kSWarps <= kConsumerWarps, "stream warps are consumer warps");
+
+// A granule's unit (row, KV head, first granule, granules) and valid tokens.
+struct SInfo {
+    int r, kvh, us, n, valid;
+};
+
+// Byte offset of the stream warps' scratch states in the workspace (after
+// the record slots of the grid's blocks and the units).
+__device__ __forceinline__ size_t stream_scratch_offset(const Params& p) {
+    const size_t rec = (size_t)kRecBytes * ((size_t)gridDim.x + (size_t)p.rows * p.hk);
+    return (rec + 255) / 256 * 256;
 }
 
-// Stream mode, consumer warps 0-3: one granule per warp per stage; at each
-// piece's end the four warps dump their states and combine them.  Records the
-// block's split pieces as merge tasks.
-template <bool kPaged, bool kFp8>
-__device__ __noinline__ void stream_consume(const Params& p, const Ctx& cx, int cta, int warp,
-                                            int lane) {
-    const int tid = threadIdx.x, rows = p.rows, hk = p.hk;
-    const BlockPlan* bpc = cx.bp;
-    BlockPlan* bp = cx.bp;
-    const int g0 = bpc->g0, g1 = bpc->g1;
-    const int* sm_pre = cx.pre;
-    int* sm_ppos = cx.ppos;
-    volatile int* sm_flags = cx.flags;
-    unsigned char* smem = cx.smem;
-    const uint32_t sbase = cx.sbase, bar_full = cx.bar_full, bar_empty = cx.bar_empty;
-    const bool fused = kPaged && p.positions != nullptr;
-    const int gq = lane >> 2, tq = lane & 3;
-    // Append positions of this block's first pieces, read once right after
-    // the wait, so a piece never starts with a dependent global load.
-    if (fused) {
-        if (tid == 0) {
-            int lo = 0, hi = rows - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (sm_pre[mid] <= g0) lo = mid; else hi = mid - 1;
-            }
-            int r = lo, n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-            int kvh = (g0 - sm_pre[r]) / n, us = sm_pre[r] + kvh * n, k = 0;
-            for (int g = g0; g < g1 && k < kMaxPieces;) {
-                sm_ppos[k++] = r;  // row of piece k (replaced by its position below)
-                g = min(g1, us + n);
-                if (g >= g1) break;
-                if (kvh + 1 < hk) {
-                    ++kvh;
-                    us += n;
-                } else {
-                    ++r;
-                    while (r < rows - 1 && sm_pre[r + 1] == sm_pre[r]) ++r;
-                    kvh = 0;
-                    n = (sm_pre[r + 1] - sm_pre[r]) / hk;
-                    us = sm_pre[r];
-                }
-            }
-            sm_flags[2] = k;
-        }
-        named_sync(kBarStream, kStreamWarps * 32);
+// Granule gg's unit, valid tokens and physical row (-1: a bad table entry,
+// flagged; nothing is read for it).
+__device__ __forceinline__ void resolve_granule(const Params& p, bool paged, const int* sm_pre,
+                                                const int* sm_len, int gg, SInfo& gi, int& zrow) {
+    int lo = 0, hi = p.rows - 1;
+#pragma unroll 1
+    while (lo < hi) {  // largest row with sm_pre[row] <= gg
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm_pre[mid] <= gg) lo = mid; else hi = mid - 1;
     }
-    // Each thread's position load stays in flight while the first tile lands;
-    // it is published to shared memory after the first full barrier.
-    const int npp = fused ? sm_flags[2] : 0;
-    const int my_pos = tid < npp ? p.positions[sm_ppos[tid]] : 0;
-    bool pos_published = !fused;
-    int piece = 0;
+    const int r = lo;
+    const int n = (sm_pre[r + 1] - sm_pre[r]) / p.hk;
+    const int kvh = (gg - sm_pre[r]) / n;
+    const int us = sm_pre[r] + kvh * n;
+    const int tok = (gg - us) * kGranule;
+    int valid = min(kGranule, sm_len[r] - tok);
+    if (valid < 0) valid = 0;
+    if (paged) {
+        const int pb = p.tables[(int64_t)r * p.mbpr + tok / p.bs];
+        if (pb < 0 || pb >= p.nb) {
+            flag_error(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+            valid = 0;
+            zrow = -1;
+        } else {
+            zrow = pb * p.bs + tok % p.bs;
+        }
+    } else {
+        zrow = r * p.width + tok;
+    }
+    gi.r = r;
+    gi.kvh = kvh;
+    gi.us = us;
+    gi.n = n;
+    gi.valid = valid;
+}
 
-    uint32_t qb[16];
+// Writes a warp's state (l reduced) to global memory in the dump layout.
+__device__ __forceinline__ void dump_state_global(const Soft& st, unsigned char* dump, int lane) {
+    if (lane < 4) *reinterpret_cast<float4*>(dump + 16 * lane) = make_float4(st.m0, st.m1, st.l0, st.l1);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(dump + kMlBytes + c * kChunkBytes + lane * 16) =
+            make_float4(st.o[c][0], st.o[c][1], st.o[c][2], st.o[c][3]);
+}
+
+// The granule share [wa, wb) of stream warp w.
+__device__ __forceinline__ void stream_share(int g0, int g1, int w, int& wa, int& wb) {
+    const int ng = g1 - g0;
+    wa = g0 + (int)((int64_t)ng * w / kSWarps);
+    wb = g0 + (int)((int64_t)ng * (w + 1) / kSWarps);
+}
+
+template <bool kPaged, bool kFp8>
+__device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta, int warp, int lane,
+                                         unsigned char* scratch) {
+    constexpr int kRowBytes = kFp8 ? 128 : 256;  // one token of one KV head
+    BlockPlan* bp = cx.bp;
+    const int g0 = bp->g0, g1 = bp->g1, hk = p.hk;
+    const int* sm_pre = cx.pre;
+    const int* sm_len = cx.len;
+    unsigned char* smem = cx.smem;
+    int* sinfo = reinterpret_cast<int*>(smem + Smem::sinfo) + warp * kSSlots;  // packed unit of each slot
+    const uint32_t slot0 = cx.sbase + Smem::ring + warp * kSSlots * kSlotBytes;
+    const unsigned char* kpool = reinterpret_cast<const unsigned char*>(p.kbase);
+    const unsigned char* vpool = reinterpret_cast<const unsigned char*>(p.vbase);
+    const uint32_t rstride = (uint32_t)hk * kRowBytes;
+    const bool fused = kPaged && p.positions != nullptr;
+    int wa, wb;
+    stream_share(g0, g1, warp, wa, wb);
+
+    // Lane j resolves granule bb + j of the share, 32 at a time: the byte
+    // offset of its first token's row for its KV head (-1: a bad table entry)
+    // and its row | KV head << 16 | valid tokens << 24.
+    int bb = wa, pinfo = 0;
+    long long koff = 0;
+    auto resolve = [&]() {
+        if (lane < wb - bb) {
+            SInfo x;
+            int zrow = 0;
+            resolve_granule(p, kPaged, sm_pre, sm_len, bb + lane, x, zrow);
+            koff = zrow < 0 ? -1ll : ((long long)zrow * hk + x.kvh) * kRowBytes;
+            pinfo = x.r | (x.kvh << 16) | ((zrow < 0 ? 0 : x.valid) << 24);
+        }
+    };
+    resolve();
+    const int fpi = __shfl_sync(0xffffffffu, pinfo, 0);
+    const int fr = fpi & 0xffff, fkvh = (fpi >> 16) & 0xff;
+    const int fn = (sm_pre[fr + 1] - sm_pre[fr]) / hk, fus = sm_pre[fr] + fkvh * fn;
+    auto issue = [&](int g) {
+        if (g >= bb + 32) {  // the next 32 granules
+            bb += 32;
+            resolve();
+        }
+        const int j = g - bb;
+        const long long off = __shfl_sync(0xffffffffu, koff, j);
+        const int pi = __shfl_sync(0xffffffffu, pinfo, j);
+        const int s = (g - wa) % kSSlots;
+        stage_rows<kFp8>(slot0 + s * kSlotBytes, kpool, vpool, off < 0 ? 0 : off, rstride, pi >> 24, lane);
+        if (lane == 0) sinfo[s] = pi;
+    };
+    // the first granules' copies go out before the dependency wait
+#pragma unroll 1
+    for (int g = wa; g < wa + kSDepth; ++g) {
+        if (g < wb) issue(g);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    {
+        // warm L2 with the first unit's query rows (read after the wait)
+        const char* qrow = reinterpret_cast<const char*>(p.q + ((int64_t)fr * p.hq + fkvh * p.group) * kHeadDim);
+        if (lane < 2 * p.group) asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + lane * 128));
+    }
+    // Everything below may read what the preceding kernel wrote (query,
+    // positions, new tokens, workspace) or write what it reads.
+    griddep_wait();
+
     Soft st;
-    st.reset();
-    int patch_tok = -1;  // unit-local token this piece must take from k_new / v_new
+    int cu = -1, cr = 0, ckvh = 0, cus = 0, cn = 0;  // the unit being accumulated
+    bool parked = false;  // this warp's first unit waits in its scratch slot
+    uint32_t qb[16];
+    int patch_tok = -1;
     uint4 patch_val = make_uint4(0, 0, 0, 0);
-    int tile = 0;
-    while (true) {
-        const int s = tile % kStages;
-        const uint32_t round = (uint32_t)tile / kStages;
-        if (!mbar_wait(bar_full + 8 * s, round & 1)) {
-            if (lane == 0) {
-                sm_flags[0] = 1;
-                flag_error(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            }
-            break;
-        }
-        if (!pos_published) {
-            if (tid < npp) sm_ppos[tid] = my_pos;
-            named_sync(kBarStream, kStreamWarps * 32);
-            pos_published = true;
-        }
-        const TileDesc* d = cx.desc + s;
-        const int flags = d->flags;
-        if (flags & kEnd) break;
-        const int r = d->r, kvh = d->kvh, ng = d->ng, tok0 = d->tok0;
-        const int ustart = d->ustart, n = d->n, pend = d->pend;
-        const int valid = warp < ng ? d->valid[warp] : 0;
-        if (flags & kFirst) {
-            load_q(qb, reinterpret_cast<const uint32_t*>(smem + Smem::q + s * kQBytes + gq * 256),
-                   gq < p.group, tq);
-            st.reset();
-            patch_tok = -1;
-            const int this_piece = piece++;
-            if (fused) {
-                // The appended token, if it falls inside this piece, is taken from
-                // k_new / v_new (its slot may be written concurrently).
-                const int pos = this_piece < kMaxPieces ? sm_ppos[this_piece] : p.positions[r];
-                const int pg = pos >= 0 ? ustart + pos / kGranule : -1;
-                if (pos >= 0 && pg >= ustart + tok0 / kGranule && pg < pend) {
-                    patch_tok = pos;
-                    const int chunk = lane & 15;
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
-                    patch_val = src[chunk];
-                    if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? cx.ks[kvh] : cx.vs[kvh]));
-                }
-            }
-        }
-        bool wrote = false;
-        if (warp < ng) {
-            const int gtok = tok0 + warp * kGranule;  // unit-local token of this granule
-            const int si = s * kTileGranules + warp;
-            if (kFp8) widen_fp8_slot(smem + Smem::ring + si * kSlotBytes, lane);
-            wrote = kFp8 | prepare_granule(smem + Smem::ring + si * kSlotBytes, valid,
-                                           patch_tok >= 0 ? patch_tok - gtok : -1, patch_val, lane);
-            if (wrote) __syncwarp();
-            attend(st, qb, sbase + Smem::ring + si * kSlotBytes, valid,
-                   kFp8 ? p.scale_log2 * cx.ks[kvh] : p.scale_log2, lane);
-        }
-        ++tile;
-        if (!(flags & kLast)) {
-            // Generic-proxy writes must be ordered before TMA reuses the slot.
-            if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-            continue;
-        }
-
-        // ---- end of a piece: the four warps dump their states into their
-        // slots of this stage, which stays held until every warp has
-        // read them; warp j combines chunks j and j + 4 of all four ----
+    float sl2 = p.scale_log2;
+    auto finish = [&](bool at_end) {
         st.reduce_l();
         __syncwarp();
-        dump_state(st, smem + Smem::ring + (s * kTileGranules + warp) * kSlotBytes, lane);
-        named_sync(kBarStream, kStreamWarps * 32);
-        const int cs = owner_of(ustart, cx.W, cx.Geff);
-        const int P = owner_of(ustart + n - 1, cx.W, cx.Geff) - cs + 1;
-        {
-            const PieceOut po = piece_out(p, r, kvh, cs, P, cta, kFp8 ? cx.vs[kvh] : 1.f);
-            combine_dumps(po, smem + Smem::ring, nullptr, s * kTileGranules, kStreamWarps, warp, lane);
+        if (cus >= wa && cus + cn <= wb) {
+            // the whole unit lies in this share: its output, straight from registers
+            const PieceOut po = piece_out(p, cr, ckvh, 0, 1, 0, kFp8 ? cx.vs[ckvh] : 1.f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) emit_chunk(po, c, st.o[c], st.l0, st.l1, lane);
+        } else if (!at_end) {
+            dump_state_global(st, scratch, lane);  // the first unit, shared with earlier warps or blocks
+            parked = true;
+        } else {
+            dump_state(st, smem + Smem::ring + warp * kSSlots * kSlotBytes, lane);
         }
-        // Generic-proxy writes must be ordered before TMA reuses the slots.
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    };
+#pragma unroll 1
+    for (int g = wa; g < wb; ++g) {
+        if (g + kSDepth < wb) issue(g + kSDepth);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group %0;" ::"n"(kSDepth) : "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (P > 1 && tid == 0) {
-            // A contiguous range has at most two split pieces: its first and its last.
-            const int k = bp->ntasks;
+        const int s = (g - wa) % kSSlots;
+        const int pi = sinfo[s];
+        const int u = pi & 0xffffff;  // row | KV head << 16
+        const int valid = pi >> 24;
+        if (u != cu) {
+            if (cu >= 0) finish(false);
+            cu = u;
+            cr = pi & 0xffff;
+            ckvh = (pi >> 16) & 0xff;
+            cn = (sm_pre[cr + 1] - sm_pre[cr]) / hk;
+            cus = sm_pre[cr] + ckvh * cn;
+            st.reset();
+            load_q_global(qb, p.q + ((int64_t)cr * p.hq + ckvh * p.group) * kHeadDim, p.group, lane);
+            if (kFp8) sl2 = p.scale_log2 * cx.ks[ckvh];
+            patch_tok = -1;
+            if (fused) {
+                // the appended token, if its granule is in this share, comes from k_new / v_new
+                const int pos = p.positions[cr];
+                const int pg = pos >= 0 ? cus + pos / kGranule : -1;
+                if (pos >= 0 && pg >= (cus > wa ? cus : wa) && pg < (cus + cn < wb ? cus + cn : wb)) {
+                    patch_tok = pos;
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        (lane < 16 ? p.k_new : p.v_new) + ((int64_t)cr * hk + ckvh) * kHeadDim);
+                    patch_val = src[lane & 15];
+                    if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? cx.ks[ckvh] : cx.vs[ckvh]));
+                }
+            }
+        }
+        unsigned char* sp = smem + Smem::ring + (warp * kSSlots + s) * kSlotBytes;
+        if (kFp8) widen_fp8_slot(sp, lane);
+        const int prow = patch_tok >= 0 ? patch_tok - (g - cus) * kGranule : -1;
+        if (prow >= 0 && prow < valid) {
+            // the appended token's row, in the fp16 slot layout
+            const int c16 = lane & 15;
+            unsigned char* box = sp + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
+            *reinterpret_cast<uint4*>(box + prow * 128 + (((c16 & 7) ^ (prow & 7)) << 4)) = patch_val;
+        }
+        __syncwarp();
+        attend(st, qb, slot0 + s * kSlotBytes, valid, sl2, lane);
+        __syncwarp();  // the slot is read before its next copy is issued
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (cu >= 0) finish(true);
+    if (parked) {
+        // back into slot 1 for the combine (written by this warp above)
+        __syncwarp();
+        const uint4* src = reinterpret_cast<const uint4*>(scratch);
+        uint4* dst = reinterpret_cast<uint4*>(smem + Smem::ring + (warp * kSSlots + 1) * kSlotBytes);
+#pragma unroll 1
+        for (int i = lane; i < (int)(kStateBytes / 16); i += 32) dst[i] = src[i];
+    }
+    named_sync(kBarStream, kSWarps * 32);
+
+    // ---- combine: every unit of the block that is not whole in one share,
+    // by the warps that hold its states ----
+#pragma unroll 1
+    for (int side = 0; side < 2; ++side) {
+        // this warp's first unit, then its last one
+        const int xr = side ? cr : fr, xkvh = side ? ckvh : fkvh;
+        const int xus = side ? cus : fus, xn = side ? cn : fn;
+        if (side == 1 && xus == fus && xr == fr && xkvh == fkvh) continue;  // the same unit
+        if (xus >= wa && xus + xn <= wb) continue;                          // whole: done
+        // warps a .. b hold the unit's states
+        int a = 0, b = kSWarps - 1;
+#pragma unroll 1
+        for (int w = 0; w < kSWarps; ++w) {
+            int xa, xb;
+            stream_share(g0, g1, w, xa, xb);
+            if (xb <= xus) a = w + 1;
+            if (xa >= xus + xn && b == kSWarps - 1 && w > 0) b = w - 1;
+        }
+        int slot[kConsumerWarps];
+#pragma unroll
+        for (int i = 0; i < kConsumerWarps; ++i) slot[i] = 0;
+#pragma unroll 1
+        for (int w = a; w <= b; ++w) {
+            int xa, xb;
+            stream_share(g0, g1, w, xa, xb);
+            // a unit that started before the warp's share and ends inside it
+            // is the warp's first unit, finished early and parked
+            const bool early = xus < xa && xus + xn < xb;
+            slot[w - a] = w * kSSlots + (early ? 1 : 0);
+        }
+        const int cs = owner_of(xus, cx.W, cx.Geff);
+        const int P = owner_of(xus + xn - 1, cx.W, cx.Geff) - cs + 1;
+        const PieceOut po = piece_out(p, xr, xkvh, cs, P, cta, kFp8 ? cx.vs[xkvh] : 1.f);
+        combine_dumps(po, smem + Smem::ring, slot, b - a + 1, warp - a, lane);
+        if (P > 1 && warp == a && lane == 0) {
+            // the block's split pieces (its first and its last) are its merge tasks
+            const int k = atomicAdd(&bp->ntasks, 1);
             if (k < kMaxTasks) {
                 Task& t = bp->tasks[k];
-                t.u = r * hk + kvh;
+                t.u = xr * hk + xkvh;
                 t.cs = cs;
                 t.P = P;
                 t.idx = cta - cs;
-                t.r = r;
-                t.kvh = kvh;
-                bp->ntasks = k + 1;
+                t.r = xr;
+                t.kvh = xkvh;
             }
         }
     }
-    // the ring is idle once every stage is consumed
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    named_sync(kBarStream, kStreamWarps * 32);
+    named_sync(kBarStream, kSWarps * 32);
 }
 
 // Burst mode, warp j of piece k's n warps (n > 1): chunks c = j, j + n, ...
@@ -1376,8 +1318,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Params& p = prm;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + Smem::bars;
-    const uint32_t bar_empty = bar_full + kStages * 8;
     BlockPlan* bp = reinterpret_cast<BlockPlan*>(smem + Smem::plan);
     volatile int* sm_flags = reinterpret_cast<volatile int*>(smem + Smem::flags);
     int* sm_part = reinterpret_cast<int*>(smem + Smem::part);
@@ -1431,31 +1371,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int mode = bp->mode;
     const int g0 = bp->g0;
-    if (mode == kModeStream) {
-        // only stream mode uses the stage barriers and the tiled copies
-        if (tid == 0) {
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(bar_full + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, kStreamWarps);
-            }
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            // fetch the tensor-map descriptors now; the first copy would wait for them
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
-        }
-        __syncthreads();
-    }
     Ctx cx;
     cx.smem = smem;
     cx.sbase = sbase;
-    cx.bar_full = bar_full;
-    cx.bar_empty = bar_empty;
     cx.bp = bp;
     cx.flags = sm_flags;
-    cx.desc = reinterpret_cast<TileDesc*>(smem + Smem::desc);
     cx.pre = sm_pre;
     cx.len = sm_len;
-    cx.ppos = reinterpret_cast<int*>(smem + Smem::ppos);
     cx.ks = sm_ks;
     cx.vs = sm_vs;
     cx.W = W;
@@ -1463,10 +1385,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ============================ producer ============================
-        if (mode == kModeStream) {
-            stream_produce<kPaged, kFp8>(&kmap, &vmap, p, cx, cta, lane);
-            return;
-        }
         // Burst (or idle): the consumer warps stage their own granules; this
         // warp only does the block's row work after the dependency wait.
         griddep_wait();
@@ -1476,9 +1394,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ============================== consumers ==============================
     if (mode == kModeStream) {
-        if (warp >= kStreamWarps) return;  // stream mode runs on warps 0-3
-        griddep_wait();
-        stream_consume<kPaged, kFp8>(p, cx, cta, warp, lane);
+        if (warp >= kSWarps) return;  // stream mode runs on warps 0 .. kSWarps-1
+        stream_warp<kPaged, kFp8>(p, cx, cta, warp, lane,
+                                  p.records + stream_scratch_offset(p) + ((size_t)cta * kSWarps + warp) * kStateBytes);
     } else {
         // ============================ burst mode ============================
         const int pi = bp->wpiece[warp];
@@ -1594,7 +1512,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (ntask == 0) return;
     const bool burst = mode == kModeBurst;
-    const int nc = burst ? kConsumerWarps : kStreamWarps;
+    const int nc = burst ? kConsumerWarps : kSWarps;
     const int half = nc / 2;
     const int t = ntask == 1 ? first : (warp < half ? 0 : 1);
     const int lw = (ntask == 1 || warp < half) ? warp : warp - half;
@@ -1700,7 +1618,11 @@ static int64_t tma_slots(int rows, int kv_heads, int max_seq_len) {
 
 size_t tma_workspace_bytes(int rows, int q_heads, int kv_heads, int max_seq_len) {
     (void)q_heads;
-    return align_up((size_t)tma::kRecBytes * (size_t)tma_slots(rows, kv_heads, max_seq_len), 256);
+    // the records, then one parked state per stream warp of every block
+    int ctas = tma::kMaxCtas;
+    if (tma::decode_grid(rows, kv_heads, max_seq_len, &ctas) != PKV_OK) ctas = tma::kMaxCtas;
+    return align_up((size_t)tma::kRecBytes * (size_t)tma_slots(rows, kv_heads, max_seq_len), 256) +
+           (size_t)ctas * tma::kSWarps * tma::kStateBytes;
 }
 
 size_t tma_plan_bytes(int rows, int kv_heads, int max_seq_len) {
