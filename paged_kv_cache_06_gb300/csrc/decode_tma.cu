@@ -1413,6 +1413,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     bp->skvh[si], zrow < 0 ? 0 : bp->svalid[si], lane);
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
+            if (kFp8) {
+                // the copies land before the dependency releases: widen the
+                // E4M3 slots to fp16 now, off the critical path
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll 1
+                for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g)
+                    widen_fp8_slot(smem + Smem::ring + (g - g0) * kSlotBytes, lane);
+            }
             // Warm L2 with this warp's query rows and new token.  A prefetch
             // reads nothing into the block, so it may precede the dependency
             // wait: the values used are loaded after it.
@@ -1460,7 +1469,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int g = a; g < b; ++g) {
                 const int si = g - g0;
                 unsigned char* sp = smem + Smem::ring + si * kSlotBytes;
-                if (kFp8) widen_fp8_slot(sp, lane);
                 const int prow = patch_tok >= 0 ? patch_tok - (g - us) * kGranule : -1;
                 if (prow >= 0 && prow < bp->svalid[si]) {
                     // the appended token's row, in the fp16 slot layout
