@@ -80,6 +80,7 @@ namespace tma {
 constexpr int kGranule = 16;        // tokens per box and per consumer warp step
 constexpr int kRing = 12;           // granule slots
 constexpr int kConsumerWarps = 7;   // burst mode
+constexpr int kStreamWarps = 4;     // stream mode: warps 0-3 stream, each through three slots
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kMaxCtas = 1024;
@@ -545,32 +546,33 @@ __device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, 
                M1, L0, L1);
 }
 
-// Warp j of a piece's k warps (k <= kConsumerWarps), whose states are dumped
-// in ring slots slot[0 .. k-1]: combines them through their log-sum-exp for
-// chunks c = j, j + k, ... and emits those; warp 0 also emits the m/l.  Every
+// Stream mode, warp j of the k stream warps (k <= kStreamWarps) holding a
+// unit's states, dumped in ring slots slot[0 .. k-1]: combines them through
+// their log-sum-exp for chunks c = j, j + k, ... and emits those; warp 0 also
+// emits the m/l.  Every
 // state's offset, maximum and sum is loaded up front, the weights are
 // computed once, and each chunk's k loads are issued together, so the chains
 // overlap.
 __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring,
-                              const int (&slot)[kConsumerWarps], int k, int j, int lane) {
+                              const int (&slot)[kStreamWarps], int k, int j, int lane) {
     const int tq = lane & 3;
-    uint32_t off[kConsumerWarps];
+    uint32_t off[kStreamWarps];
 #pragma unroll
-    for (int s = 0; s < kConsumerWarps; ++s) off[s] = (uint32_t)slot[s < k ? s : 0] * kSlotBytes;
-    float4 ml[kConsumerWarps];
+    for (int s = 0; s < kStreamWarps; ++s) off[s] = (uint32_t)slot[s < k ? s : 0] * kSlotBytes;
+    float4 ml[kStreamWarps];
 #pragma unroll
-    for (int s = 0; s < kConsumerWarps; ++s)
+    for (int s = 0; s < kStreamWarps; ++s)
         ml[s] = s < k ? *reinterpret_cast<const float4*>(ring + off[s] + 16 * tq)
                       : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
     float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kConsumerWarps; ++s) {
+    for (int s = 0; s < kStreamWarps; ++s) {
         M0 = fmaxf(M0, ml[s].x);
         M1 = fmaxf(M1, ml[s].y);
     }
     float L0 = 0.f, L1 = 0.f;
 #pragma unroll
-    for (int s = 0; s < kConsumerWarps; ++s) {  // ml[s].x / .y become the weights
+    for (int s = 0; s < kStreamWarps; ++s) {  // ml[s].x / .y become the weights
         ml[s].x = M0 == -INFINITY ? 0.f : fast_exp2(ml[s].x - M0);
         ml[s].y = M1 == -INFINITY ? 0.f : fast_exp2(ml[s].y - M1);
         L0 += ml[s].x * ml[s].z;
@@ -578,14 +580,14 @@ __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring,
     }
 #pragma unroll 1
     for (int c = j; c < 8; c += k) {
-        float4 v[kConsumerWarps];
+        float4 v[kStreamWarps];
 #pragma unroll
-        for (int s = 0; s < kConsumerWarps; ++s)
+        for (int s = 0; s < kStreamWarps; ++s)
             v[s] = s < k ? *reinterpret_cast<const float4*>(ring + off[s] + kMlBytes + c * kChunkBytes + lane * 16)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s = 0; s < kConsumerWarps; ++s) {
+        for (int s = 0; s < kStreamWarps; ++s) {
             acc[0] += ml[s].x * v[s].x;
             acc[1] += ml[s].y * v[s].y;
             acc[2] += ml[s].x * v[s].z;
@@ -999,7 +1001,7 @@ struct Ctx {
 // into its slot 1 at the end).  After a barrier of the stream warps each such
 // unit is combined by the warps that hold its states and emitted (fp16
 // output, or the block's record of a split unit), as in burst mode.
-constexpr int kSWarps = 4;                 // stream warps
+constexpr int kSWarps = kStreamWarps;      // stream warps
 constexpr int kSSlots = kRing / kSWarps;   // ring slots per stream warp
 constexpr int kSDepth = kSSlots - 1;       // copies in flight ahead of the granule consumed
 static_assert(kSSlots >= 2 && kSWarps * kSSlots == kRing, "stream slots");
@@ -1231,9 +1233,9 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
             if (xb <= xus) a = w + 1;
             if (xa >= xus + xn && b == kSWarps - 1 && w > 0) b = w - 1;
         }
-        int slot[kConsumerWarps];
+        int slot[kSWarps];
 #pragma unroll
-        for (int i = 0; i < kConsumerWarps; ++i) slot[i] = 0;
+        for (int i = 0; i < kSWarps; ++i) slot[i] = 0;
 #pragma unroll 1
         for (int w = a; w <= b; ++w) {
             int xa, xb;
@@ -1413,15 +1415,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     bp->skvh[si], zrow < 0 ? 0 : bp->svalid[si], lane);
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
-            if (kFp8) {
-                // the copies land before the dependency releases: widen the
-                // E4M3 slots to fp16 now, off the critical path
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
-                __syncwarp();
-#pragma unroll 1
-                for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g)
-                    widen_fp8_slot(smem + Smem::ring + (g - g0) * kSlotBytes, lane);
-            }
             // Warm L2 with this warp's query rows and new token.  A prefetch
             // reads nothing into the block, so it may precede the dependency
             // wait: the values used are loaded after it.
@@ -1433,6 +1426,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const char* nt = reinterpret_cast<const char*>(
                     (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
+            }
+            if (kFp8) {
+                // the copies land before the dependency releases: widen the
+                // E4M3 slots to fp16 now, off the critical path
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll 1
+                for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g)
+                    widen_fp8_slot(smem + Smem::ring + (g - g0) * kSlotBytes, lane);
             }
         }
         // Everything below may read what the preceding kernel wrote (query,
