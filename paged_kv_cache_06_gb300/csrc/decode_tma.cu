@@ -1532,8 +1532,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                kFp8 ? sm_vs[task.kvh] : 1.f, sm_flags + 4 + t, lane);
 }
 
-// The plan of a step: one block scans the lengths once, then warp w makes
-// the plans of blocks w, w + 32, ... and copies each out as 32 x 16 bytes.
+// The plan of a step: every block scans the lengths, then warp w of block i
+// makes the plan of decode block 32 i + w (and of those a grid stride
+// further) and copies it out as 32 x 16 bytes.
 __global__ void __launch_bounds__(kPlanThreads, 1)
     decode_plan_kernel(const Params p, unsigned char* plan, int G) {
     extern __shared__ __align__(16) unsigned char psm[];
@@ -1541,10 +1542,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     int* part = reinterpret_cast<int*>(psm + (kPlanThreads / 32) * kPlanBytes);
     int* pre = part + kPlanThreads;
     int* len = pre + p.rows + 1;
-    const int W = scan_lengths<kPlanThreads>(p, true, pre, len, part, true);
+    const int W = scan_lengths<kPlanThreads>(p, true, pre, len, part, blockIdx.x == 0);
     const int Geff = W < G ? W : G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int b = warp; b < G; b += kPlanThreads / 32) {
+    for (int b = blockIdx.x * (kPlanThreads / 32) + warp; b < G; b += gridDim.x * (kPlanThreads / 32)) {
         build_block_plan(bps + warp, p, true, b, G, W, Geff, pre, len, lane);
         reinterpret_cast<uint4*>(plan + (size_t)b * kPlanBytes)[lane] =
             reinterpret_cast<const uint4*>(bps + warp)[lane];
@@ -1665,7 +1666,8 @@ int tma_plan_launch(void* plan, size_t plan_bytes, const int32_t* tables, const 
     prm.dev_err = dev_err;
     prm.positions = positions;
     const size_t smem = (kPlanThreads / 32) * kPlanBytes + kPlanThreads * 4 + (size_t)(2 * rows + 1) * 4;
-    decode_plan_kernel<<<1, kPlanThreads, smem, stream>>>(prm, static_cast<unsigned char*>(plan), G);
+    decode_plan_kernel<<<(G + kPlanThreads / 32 - 1) / (kPlanThreads / 32), kPlanThreads, smem, stream>>>(
+        prm, static_cast<unsigned char*>(plan), G);
     return launch_status();
 }
 
