@@ -235,30 +235,30 @@ struct Soft {
     }
 };
 
-// One online-softmax step of a warp over the granule staged at `slot` (K dims
-// 0-63 at +0, K 64-127 at +2 KB, V at +4 KB / +6 KB, 128-byte swizzled rows)
-// with `valid` tokens.  Rows past `valid` must hold finite values (zeroed by
-// the caller) so that 0 * V stays 0.
-__device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint32_t slot, int valid,
-                                       float scale_log2, int lane) {
-    const int gq = lane >> 2;
-    float s[4];
-    {
-        // S^T = K . Q^T; two independent chains (even / odd k-steps)
-        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int chunk = (ks & 3) * 2 + (lane >> 4);
-            const uint32_t off = (ks >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(slot + off, a0, a1, a2, a3);
-            mma16816((ks & 1) ? c1 : c0, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[i] = c0[i] + c1[i];
+// Writes the appended token's row `prow` into a staged slot: lanes 0-15
+// carry its K, lanes 16-31 its V, each lane one 16-byte chunk of fp16 dims
+// 8c..8c+7 (c = lane % 16), or, for FP8 pools, those dims' 8 codes in the
+// low 8 bytes.
+template <bool kFp8>
+__device__ __forceinline__ void patch_row(unsigned char* sp, int prow, const uint4& v, int lane) {
+    const int c16 = lane & 15;
+    if (kFp8) {
+        unsigned char* box = sp + (lane < 16 ? 0u : kBoxBytes);
+        *reinterpret_cast<uint2*>(box + prow * 128 + ((((c16 >> 1) ^ (prow & 7)) << 4) | ((c16 & 1) << 3))) =
+            make_uint2(v.x, v.y);
+    } else {
+        unsigned char* box = sp + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
+        *reinterpret_cast<uint4*>(box + prow * 128 + (((c16 & 7) ^ (prow & 7)) << 4)) = v;
     }
-    // scores: s0 = (tok gq, head 2tq), s1 = (gq, 2tq+1), s2/3 = tok gq+8
+}
+
+// The online-softmax step of a warp on its granule's scores S^T (s0 = token
+// gq, head 2tq; s1 = gq, 2tq+1; s2, s3 = token gq+8) with `valid` tokens:
+// updates the running max and sum, rescales O and returns the B fragments
+// of P^T (token x head) for the PV product.
+__device__ __forceinline__ void softmax_step(Soft& st, float (&s)[4], int valid, float scale_log2,
+                                             int lane, uint32_t& pb0, uint32_t& pb1) {
+    const int gq = lane >> 2;
     s[0] = gq < valid ? s[0] * scale_log2 : -INFINITY;
     s[1] = gq < valid ? s[1] * scale_log2 : -INFINITY;
     s[2] = gq + 8 < valid ? s[2] * scale_log2 : -INFINITY;
@@ -283,7 +283,8 @@ __device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint3
     st.l0 = st.l0 * al0 + (fx.x + fy.x);
     st.l1 = st.l1 * al1 + (fx.y + fy.y);
     // B fragments of P^T (token x head) by transposing in registers
-    const uint32_t pb0 = movmatrix_t(px), pb1 = movmatrix_t(py);
+    pb0 = movmatrix_t(px);
+    pb1 = movmatrix_t(py);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         st.o[i][0] *= al0;
@@ -291,6 +292,31 @@ __device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint3
         st.o[i][2] *= al0;
         st.o[i][3] *= al1;
     }
+}
+
+// One online-softmax step of a warp over the fp16 granule staged at `slot`
+// (K dims 0-63 at +0, K 64-127 at +2 KB, V at +4 KB / +6 KB, 128-byte
+// swizzled rows) with `valid` tokens.  Rows past `valid` hold zeros.
+__device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint32_t slot, int valid,
+                                       float scale_log2, int lane) {
+    float s[4];
+    {
+        // S^T = K . Q^T; two independent chains (even / odd k-steps)
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int chunk = (ks & 3) * 2 + (lane >> 4);
+            const uint32_t off = (ks >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(slot + off, a0, a1, a2, a3);
+            mma16816((ks & 1) ? c1 : c0, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] = c0[i] + c1[i];
+    }
+    uint32_t pb0, pb1;
+    softmax_step(st, s, valid, scale_log2, lane, pb0, pb1);
     // O^T += V^T . P^T
     const int row = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
@@ -299,6 +325,65 @@ __device__ __forceinline__ void attend(Soft& st, const uint32_t (&qb)[16], uint3
         const uint32_t off = kSlotV + (mt >> 2) * kBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(slot + off, a0, a1, a2, a3);
+        mma16816(st.o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+}
+
+// The same over an FP8 granule at `slot` (E4M3 K box at +0, V box at +2 KB,
+// 16 rows x 128 bytes, 128-byte swizzled), converting E4M3 to fp16 in
+// registers (exact) as the fragments are built.  The dot product runs over
+// the dims in a per-lane order: k-step ks of lane (g, t) takes dims 32t + 4ks
+// .. 32t + 4ks + 3 (its 4-byte word ks of K rows g and g + 8), so the queries
+// come in the same order (load_q_fp8).  The output dims are ordered per lane
+// too: row g of m-tile i is dim 16g + 2i and row g + 8 is 16g + 2i + 1, so
+// lane (g, t) reads one 16-byte chunk of each of its four V rows
+// (store_chunk_fp8 writes the result back in natural order).
+__device__ __forceinline__ void attend8(Soft& st, const uint32_t (&qb)[16], const unsigned char* slot,
+                                        int valid, float scale_log2, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float s[4];
+    {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            // bytes 32t + 16h .. +15 of K rows g and g + 8 (chunk 2t + h; (g + 8) & 7 == g)
+            const uint32_t off = ((uint32_t)(2 * t + h) ^ (uint32_t)g) << 4;
+            const uint4 r0 = *reinterpret_cast<const uint4*>(slot + g * 128 + off);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(slot + (g + 8) * 128 + off);
+            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ks = 4 * h + j;
+                uint32_t a0, a1, a2, a3;
+                widen4(w0[j], a0, a2);  // row g: dims 2t, 2t+1 | 8+2t, 9+2t of the k-step
+                widen4(w1[j], a1, a3);  // row g + 8
+                mma16816((ks & 1) ? c1 : c0, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] = c0[i] + c1[i];
+    }
+    uint32_t pb0, pb1;
+    softmax_step(st, s, valid, scale_log2, lane, pb0, pb1);
+    // O^T += V^T . P^T: chunk g (dims 16g .. 16g+15) of V rows 2t, 2t+1, 8+2t, 9+2t
+    const unsigned char* vb = slot + kBoxBytes;
+    const int ra = 2 * t;  // rows ra, ra + 1, ra + 8, ra + 9 share ra & 7 up to the low bit
+    const uint4 X = *reinterpret_cast<const uint4*>(vb + ra * 128 + (((uint32_t)g ^ (uint32_t)(ra & 7)) << 4));
+    const uint4 Y = *reinterpret_cast<const uint4*>(vb + (ra + 1) * 128 + (((uint32_t)g ^ (uint32_t)((ra + 1) & 7)) << 4));
+    const uint4 Z = *reinterpret_cast<const uint4*>(vb + (ra + 8) * 128 + (((uint32_t)g ^ (uint32_t)(ra & 7)) << 4));
+    const uint4 W = *reinterpret_cast<const uint4*>(vb + (ra + 9) * 128 + (((uint32_t)g ^ (uint32_t)((ra + 1) & 7)) << 4));
+    const uint32_t xs[4] = {X.x, X.y, X.z, X.w}, ys[4] = {Y.x, Y.y, Y.z, Y.w};
+    const uint32_t zs[4] = {Z.x, Z.y, Z.z, Z.w}, ws[4] = {W.x, W.y, W.z, W.w};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        // bytes 2mt, 2mt+1 of each row: (x, y) pairs for tokens 2t, 2t+1 and
+        // (z, w) pairs for tokens 8+2t, 9+2t
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        const uint32_t xy = __byte_perm(xs[mt >> 1], ys[mt >> 1], sel);
+        const uint32_t zw = __byte_perm(zs[mt >> 1], ws[mt >> 1], sel);
+        uint32_t a0, a1, a2, a3;
+        widen4(xy, a0, a1);  // dim 16g+2mt (row g) | dim 16g+2mt+1 (row g+8), tokens 2t, 2t+1
+        widen4(zw, a2, a3);  // the same, tokens 8+2t, 9+2t
         mma16816(st.o[mt], a0, a1, a2, a3, pb0, pb1);
     }
 }
@@ -322,6 +407,21 @@ __device__ __forceinline__ void load_q_global(uint32_t (&qb)[16], const __half* 
     for (int ks = 0; ks < 8; ++ks) {
         qb[2 * ks] = qrow[ks * 8];
         qb[2 * ks + 1] = qrow[ks * 8 + 4];
+    }
+}
+// The same in the FP8 dim order (attend8): lane (g, t) takes dims 32t ..
+// 32t + 31 of head g, so its word i is k-step i / 2's pair (i even: dims
+// 2t, 2t+1 of the step; odd: 8+2t, 9+2t).
+__device__ __forceinline__ void load_q_fp8(uint32_t (&qb)[16], const __half* q0, int group, int lane) {
+    const int h = (lane >> 2) < group ? (lane >> 2) : group - 1;
+    const uint4* qrow = reinterpret_cast<const uint4*>(q0 + h * kHeadDim + 32 * (lane & 3));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = qrow[i];
+        qb[4 * i] = v.x;
+        qb[4 * i + 1] = v.y;
+        qb[4 * i + 2] = v.z;
+        qb[4 * i + 3] = v.w;
     }
 }
 
@@ -389,47 +489,6 @@ __device__ __forceinline__ void stage_granule(uint32_t slot, const unsigned char
     stage_rows<kFp8>(slot, kpool, vpool, (zrow * hk + kvh) * kRowBytes, (uint32_t)hk * kRowBytes, valid,
                      lane);
 }
-// FP8 pools: the producer lands a granule's E4M3 K box (16 tokens x 128
-// bytes, 128-byte swizzle) at +0 and its V box at +2 KB of the slot; the
-// owning warp widens both in place to the fp16 slot layout attend expects
-// (exact: every E4M3 value is an fp16 value; the per-head scales are applied
-// to the scores and to the output instead).  All of the warp's reads happen
-// before any of its writes.
-__device__ __forceinline__ void widen_fp8_slot(unsigned char* slot, int lane) {
-    uint4 kc[4], vc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = lane + 32 * k, r = i >> 3, c = i & 7;
-        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
-        kc[k] = *reinterpret_cast<const uint4*>(slot + off);
-        vc[k] = *reinterpret_cast<const uint4*>(slot + kBoxBytes + off);
-    }
-    __syncwarp();
-    auto widen = [](uint32_t w, uint32_t& lo, uint32_t& hi) { widen4(w, lo, hi); };
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = lane + 32 * k, r = i >> 3, c = i & 7;
-        // 16 dims 16c..16c+15: fp16 chunks 2(c%4), 2(c%4)+1 of box c/4
-        const uint32_t j0 = (c & 3) * 2;
-        const uint32_t b0 = (c >> 2) * kBoxBytes + r * 128;
-        const uint32_t o0 = b0 + ((j0 ^ (r & 7)) << 4), o1 = b0 + (((j0 + 1) ^ (r & 7)) << 4);
-        uint4 a, b;
-        widen(kc[k].x, a.x, a.y);
-        widen(kc[k].y, a.z, a.w);
-        widen(kc[k].z, b.x, b.y);
-        widen(kc[k].w, b.z, b.w);
-        *reinterpret_cast<uint4*>(slot + o0) = a;
-        *reinterpret_cast<uint4*>(slot + o1) = b;
-        widen(vc[k].x, a.x, a.y);
-        widen(vc[k].y, a.z, a.w);
-        widen(vc[k].z, b.x, b.y);
-        widen(vc[k].w, b.z, b.w);
-        *reinterpret_cast<uint4*>(slot + kSlotV + o0) = a;
-        *reinterpret_cast<uint4*>(slot + kSlotV + o1) = b;
-    }
-    __syncwarp();
-}
-
 // ---------------------------------------------------------------------------
 // States in the fragment layout: dump, output, records, merge.
 
@@ -456,6 +515,16 @@ __device__ __forceinline__ void store_chunk(__half* ob, int c, const float (&o)[
         *reinterpret_cast<uint32_t*>(ob + h * kHeadDim + d) = x;
         *reinterpret_cast<uint32_t*>(ob + h * kHeadDim + d + 8) = y;
     }
+}
+// The same for a state in the FP8 dim order (attend8): chunk c of lane
+// (g, t) holds dims 16g + 2c (o[0], o[1]) and 16g + 2c + 1 (o[2], o[3]) of
+// heads 2t, 2t + 1.
+__device__ __forceinline__ void store_chunk_fp8(__half* ob, int c, const float (&o)[4], float inv0,
+                                                float inv1, int group, int lane) {
+    const int t = lane & 3, d = 16 * (lane >> 2) + 2 * c;
+    if (2 * t < group) *reinterpret_cast<uint32_t*>(ob + 2 * t * kHeadDim + d) = pack_half2(o[0] * inv0, o[2] * inv0);
+    if (2 * t + 1 < group)
+        *reinterpret_cast<uint32_t*>(ob + (2 * t + 1) * kHeadDim + d) = pack_half2(o[1] * inv1, o[3] * inv1);
 }
 
 // ---------------------------------------------------------------------------
@@ -525,12 +594,16 @@ __device__ __forceinline__ PieceOut piece_out(const Params& p, int r, int kvh, i
 
 // Chunk c of a piece's combined state (unnormalised acc, sums L0 / L1): the
 // fp16 output dims 16c.. when the unit is whole, else the record words.
+template <bool kFp8>
 __device__ __forceinline__ void emit_chunk(const PieceOut& po, int c, const float (&acc)[4], float L0,
                                            float L1, int lane) {
     if (po.P == 1) {
         const float inv0 = L0 > 0.f ? __fdividef(po.vs, L0) : 0.f;
         const float inv1 = L1 > 0.f ? __fdividef(po.vs, L1) : 0.f;
-        store_chunk(po.ob, c, acc, inv0, inv1, po.group, lane);
+        if (kFp8)  // the state is in the FP8 dim order
+            store_chunk_fp8(po.ob, c, acc, inv0, inv1, po.group, lane);
+        else
+            store_chunk(po.ob, c, acc, inv0, inv1, po.group, lane);
     } else {
         st_rec(po.region + (uint32_t)(c * po.P + po.idx) * kLLChunk + lane * 16, acc[0], acc[1], acc[2],
                acc[3]);
@@ -553,6 +626,7 @@ __device__ __forceinline__ void emit_ml(const PieceOut& po, float M0, float M1, 
 // state's offset, maximum and sum is loaded up front, the weights are
 // computed once, and each chunk's k loads are issued together, so the chains
 // overlap.
+template <bool kFp8>
 __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring,
                               const int (&slot)[kStreamWarps], int k, int j, int lane) {
     const int tq = lane & 3;
@@ -593,7 +667,7 @@ __device__ void combine_dumps(const PieceOut& po, const unsigned char* ring,
             acc[2] += ml[s].x * v[s].z;
             acc[3] += ml[s].y * v[s].w;
         }
-        emit_chunk(po, c, acc, L0, L1, lane);
+        emit_chunk<kFp8>(po, c, acc, L0, L1, lane);
     }
     if (j == 0) emit_ml(po, M0, M1, L0, L1, lane);
 }
@@ -626,6 +700,7 @@ __device__ __forceinline__ void absorb(float& M0, float& M1, float& L0, float& L
     M1 = N1;
 }
 
+template <bool kFp8>
 __device__ __forceinline__ bool merge_task(const Params& p, const Task& t, int lw, int nw,
                                            unsigned char* part, int bar_id, float vs,
                                            volatile int* fail, int lane) {
@@ -684,7 +759,11 @@ __device__ __forceinline__ bool merge_task(const Params& p, const Task& t, int l
         if (gsz == 1) {
             const float inv0 = L0 > 0.f ? __fdividef(vs, L0) : 0.f;
             const float inv1 = L1 > 0.f ? __fdividef(vs, L1) : 0.f;
-            store_chunk(p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim, t.idx + m * K, acc, inv0, inv1, p.group, lane);
+            __half* ob = p.out + ((int64_t)t.r * p.hq + t.kvh * p.group) * kHeadDim;
+            if (kFp8)
+                store_chunk_fp8(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
+            else
+                store_chunk(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
         } else {
             unsigned char* pw = part + (q * nch + m) * 1024 + lane * 16;
             *reinterpret_cast<float4*>(pw) = make_float4(M0, M1, L0, L1);
@@ -715,7 +794,10 @@ __device__ __forceinline__ bool merge_task(const Params& p, const Task& t, int l
         }
         const float inv0 = L0 > 0.f ? __fdividef(vs, L0) : 0.f;
         const float inv1 = L1 > 0.f ? __fdividef(vs, L1) : 0.f;
-        store_chunk(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
+        if (kFp8)
+            store_chunk_fp8(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
+        else
+            store_chunk(ob, t.idx + m * K, acc, inv0, inv1, p.group, lane);
     }
     return true;
 }
@@ -1148,7 +1230,7 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
             // the whole unit lies in this share: its output, straight from registers
             const PieceOut po = piece_out(p, cr, ckvh, 0, 1, 0, kFp8 ? cx.vs[ckvh] : 1.f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) emit_chunk(po, c, st.o[c], st.l0, st.l1, lane);
+            for (int c = 0; c < 8; ++c) emit_chunk<kFp8>(po, c, st.o[c], st.l0, st.l1, lane);
         } else if (!at_end) {
             dump_state_global(st, scratch, lane);  // the first unit, shared with earlier warps or blocks
             parked = true;
@@ -1174,7 +1256,10 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
             cn = (sm_pre[cr + 1] - sm_pre[cr]) / hk;
             cus = sm_pre[cr] + ckvh * cn;
             st.reset();
-            load_q_global(qb, p.q + ((int64_t)cr * p.hq + ckvh * p.group) * kHeadDim, p.group, lane);
+            if (kFp8)
+                load_q_fp8(qb, p.q + ((int64_t)cr * p.hq + ckvh * p.group) * kHeadDim, p.group, lane);
+            else
+                load_q_global(qb, p.q + ((int64_t)cr * p.hq + ckvh * p.group) * kHeadDim, p.group, lane);
             if (kFp8) sl2 = p.scale_log2 * cx.ks[ckvh];
             patch_tok = -1;
             if (fused) {
@@ -1186,21 +1271,21 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
                     const uint4* src = reinterpret_cast<const uint4*>(
                         (lane < 16 ? p.k_new : p.v_new) + ((int64_t)cr * hk + ckvh) * kHeadDim);
                     patch_val = src[lane & 15];
-                    if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? cx.ks[ckvh] : cx.vs[ckvh]));
+                    if (kFp8) {  // FP8 pools hold the token as codes
+                        const uint2 c8 = quantize8(patch_val, lane < 16 ? cx.ks[ckvh] : cx.vs[ckvh]);
+                        patch_val = make_uint4(c8.x, c8.y, 0u, 0u);
+                    }
                 }
             }
         }
         unsigned char* sp = smem + Smem::ring + (warp * kSSlots + s) * kSlotBytes;
-        if (kFp8) widen_fp8_slot(sp, lane);
         const int prow = patch_tok >= 0 ? patch_tok - (g - cus) * kGranule : -1;
-        if (prow >= 0 && prow < valid) {
-            // the appended token's row, in the fp16 slot layout
-            const int c16 = lane & 15;
-            unsigned char* box = sp + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
-            *reinterpret_cast<uint4*>(box + prow * 128 + (((c16 & 7) ^ (prow & 7)) << 4)) = patch_val;
-        }
+        if (prow >= 0 && prow < valid) patch_row<kFp8>(sp, prow, patch_val, lane);
         __syncwarp();
-        attend(st, qb, slot0 + s * kSlotBytes, valid, sl2, lane);
+        if (kFp8)
+            attend8(st, qb, sp, valid, sl2, lane);
+        else
+            attend(st, qb, slot0 + s * kSlotBytes, valid, sl2, lane);
         __syncwarp();  // the slot is read before its next copy is issued
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -1248,7 +1333,7 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
         const int cs = owner_of(xus, cx.W, cx.Geff);
         const int P = owner_of(xus + xn - 1, cx.W, cx.Geff) - cs + 1;
         const PieceOut po = piece_out(p, xr, xkvh, cs, P, cta, kFp8 ? cx.vs[xkvh] : 1.f);
-        combine_dumps(po, smem + Smem::ring, slot, b - a + 1, warp - a, lane);
+        combine_dumps<kFp8>(po, smem + Smem::ring, slot, b - a + 1, warp - a, lane);
         if (P > 1 && warp == a && lane == 0) {
             // the block's split pieces (its first and its last) are its merge tasks
             const int k = atomicAdd(&bp->ntasks, 1);
@@ -1270,6 +1355,7 @@ __device__ __noinline__ void stream_warp(const Params& p, const Ctx& cx, int cta
 // of the piece.  Combines the states the piece's warps dumped into their
 // first slots through their log-sum-exp and emits each chunk (fp16 output of
 // a whole unit, or the piece's record); warp 0 also emits a split piece's m/l.
+template <bool kFp8>
 __device__ void burst_emit(const PieceOut& po, const BlockPlan* bp, const unsigned char* ring, int k,
                            int j, int lane) {
     const int n = bp->pwn[k], w0 = bp->pw0[k], g0 = bp->g0, tq = lane & 3;
@@ -1306,7 +1392,7 @@ __device__ void burst_emit(const PieceOut& po, const BlockPlan* bp, const unsign
             acc[2] += ml[s].x * v.z;
             acc[3] += ml[s].y * v.w;
         }
-        emit_chunk(po, c, acc, L0, L1, lane);
+        emit_chunk<kFp8>(po, c, acc, L0, L1, lane);
     }
     if (j == 0) emit_ml(po, M0, M1, L0, L1, lane);
 }
@@ -1427,15 +1513,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     (lane < 4 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(nt + (lane & 3) * 64));
             }
-            if (kFp8) {
-                // the copies land before the dependency releases: widen the
-                // E4M3 slots to fp16 now, off the critical path
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
-                __syncwarp();
-#pragma unroll 1
-                for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g)
-                    widen_fp8_slot(smem + Smem::ring + (g - g0) * kSlotBytes, lane);
-            }
         }
         // Everything below may read what the preceding kernel wrote (query,
         // positions, new tokens, workspace) or write what it reads.
@@ -1448,7 +1525,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int r = bp->pr[pi], kvh = bp->pkvh[pi], us = bp->pus[pi];
             const int a = bp->wa[warp], b = bp->wb[warp];
             uint32_t qb[16];
-            load_q_global(qb, p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim, p.group, lane);
+            if (kFp8)
+                load_q_fp8(qb, p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim, p.group, lane);
+            else
+                load_q_global(qb, p.q + ((int64_t)r * p.hq + kvh * p.group) * kHeadDim, p.group, lane);
             // The appended token, if it falls inside this warp's granules, is
             // taken from k_new / v_new (its slot may be written concurrently).
             int patch_tok = -1;
@@ -1459,8 +1539,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint4* src = reinterpret_cast<const uint4*>(
                     (lane < 16 ? p.k_new : p.v_new) + ((int64_t)r * hk + kvh) * kHeadDim);
                 patch_val = src[lane & 15];
-                // FP8 pools hold the token as codes: take their exact fp16 values
-                if (kFp8) patch_val = widen8(quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]));
+                if (kFp8) {  // FP8 pools hold the token as codes
+                    const uint2 c8 = quantize8(patch_val, lane < 16 ? sm_ks[kvh] : sm_vs[kvh]);
+                    patch_val = make_uint4(c8.x, c8.y, 0u, 0u);
+                }
             }
             const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
             const bool ok = true;
@@ -1472,14 +1554,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int si = g - g0;
                 unsigned char* sp = smem + Smem::ring + si * kSlotBytes;
                 const int prow = patch_tok >= 0 ? patch_tok - (g - us) * kGranule : -1;
-                if (prow >= 0 && prow < bp->svalid[si]) {
-                    // the appended token's row, in the fp16 slot layout
-                    const int c16 = lane & 15;  // 16-byte chunk of the 128 dims
-                    unsigned char* box = sp + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
-                    *reinterpret_cast<uint4*>(box + prow * 128 + (((c16 & 7) ^ (prow & 7)) << 4)) = patch_val;
-                }
+                if (prow >= 0 && prow < bp->svalid[si]) patch_row<kFp8>(sp, prow, patch_val, lane);
                 __syncwarp();
-                attend(st, qb, sbase + Smem::ring + si * kSlotBytes, bp->svalid[si], sl2, lane);
+                if (kFp8)
+                    attend8(st, qb, sp, bp->svalid[si], sl2, lane);
+                else
+                    attend(st, qb, sbase + Smem::ring + si * kSlotBytes, bp->svalid[si], sl2, lane);
             }
             st.reduce_l();
             __syncwarp();
@@ -1495,10 +1575,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const PieceOut po = piece_out(p, r, kvh, bp->pcs[pi], bp->pP[pi], cta, kFp8 ? sm_vs[kvh] : 1.f);
                 if (k == 1) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) emit_chunk(po, c, st.o[c], st.l0, st.l1, lane);
+                    for (int c = 0; c < 8; ++c) emit_chunk<kFp8>(po, c, st.o[c], st.l0, st.l1, lane);
                     emit_ml(po, st.m0, st.m1, st.l0, st.l1, lane);
                 } else {
-                    burst_emit(po, bp, smem + Smem::ring, pi, warp - bp->pw0[pi], lane);
+                    burst_emit<kFp8>(po, bp, smem + Smem::ring, pi, warp - bp->pw0[pi], lane);
                 }
             }
         }
@@ -1528,7 +1608,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lw = (ntask == 1 || warp < half) ? warp : warp - half;
     const int nw = ntask == 1 ? nc : (t == 0 ? half : nc - half);
     const Task task = bp->tasks[t];
-    merge_task(p, task, lw, nw, smem + Smem::ring + t * kLandBytes, kBarMerge + t,
+    merge_task<kFp8>(p, task, lw, nw, smem + Smem::ring + t * kLandBytes, kBarMerge + t,
                kFp8 ? sm_vs[task.kvh] : 1.f, sm_flags + 4 + t, lane);
 }
 

@@ -2,7 +2,7 @@
 
 The append must match the oracle's quantisation bit for bit over the whole
 pool; the decode must satisfy |gpu - oracle| <= 2e-3 + 2e-3 * |oracle| like
-the fp16 decode (the kernel widens E4M3 to fp16 exactly and applies the
+the fp16 decode (the kernel converts E4M3 to fp16 exactly and applies the
 scales in fp32).
 """
 import numpy as np
@@ -77,6 +77,10 @@ def test_append_fp8_is_bit_exact_over_the_whole_pool(cuda_device, lengths, bs):
     ([5, 64, 65, 1, 4096, 300], 64),
     ([16] * 40, 16),
     ([0, 33, 2000], 32),
+    # ranges longer than the ring: stream mode, units split within and across blocks
+    ([20000, 3000, 17, 9000], 64),
+    # stream mode with several short units in every block's range
+    ([300] * 200 + [8000], 16),
 ])
 def test_decode_fp8_matches_oracle(cuda_device, lengths, bs):
     case, kp8, vp8, ks, vs = fp8_case(lengths, bs, seed=len(lengths) + bs)
@@ -149,6 +153,7 @@ def test_decode_fp8_bad_block_is_flagged(cuda_device):
     ([16] * 40, 16, True),
     ([0, 33, 2000], 32, False),
     ("mixed", 64, True),
+    ([20000, 3000, 17, 9000], 64, True),
 ])
 def test_append_decode_fp8_fused_equals_the_two_calls(cuda_device, lengths, bs, pdl):
     """One fused launch: the pools end bit-identical to the oracle's FP8
