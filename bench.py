@@ -231,6 +231,8 @@ CONFIG_DESC = {
     "shared": "96 rows log-uniform on [16, 8192], 16-token blocks, the first 592 tokens "
               "(37 blocks) shared by every row",
     "long": "4 rows x 32769 tokens (one append at 32768), 64-token blocks",
+    "uniform_fp8": "uniform, FP8 (E4M3) pools with one scale per KV head",
+    "long_fp8": "long, FP8 (E4M3) pools with one scale per KV head",
 }
 
 
@@ -290,33 +292,54 @@ def measure_configs(args, dev, peak, peak_kind):
     import torch
     from paged_kv_cache_06_gb300 import ops
     from paged_kv_cache_06_gb300 import workloads as wl
-    copies = {"tiny": 28, "uniform": 1, "shared": 4, "long": 4}
+    copies = {"tiny": 28, "uniform": 1, "shared": 4, "long": 4, "uniform_fp8": 1, "long_fp8": 4}
     out_cfg = {}
-    for name in ("tiny", "uniform", "shared", "long"):
-        if name == "uniform":
+    for name in ("tiny", "uniform", "shared", "long", "uniform_fp8", "long_fp8"):
+        fp8 = name.endswith("_fp8")
+        base = name[:-4] if fp8 else name
+        if base == "uniform":
             case = wl.uniform(seed=args.seed, layers=args.layers)
         else:
-            case = wl.WORKLOADS[name](seed=args.seed)
+            case = wl.WORKLOADS[base](seed=args.seed)
         b = wl.algorithmic_bytes(case)
+        if fp8:
+            # E4M3 codes drawn like the pools' values (scales near 1/8)
+            gen8 = torch.Generator().manual_seed(args.seed + 8)
+            k8 = [torch.from_numpy(wl.fp8_codes(gen8, case.k_pool[l].shape)) for l in range(case.layers)]
+            v8 = [torch.from_numpy(wl.fp8_codes(gen8, case.v_pool[l].shape)) for l in range(case.layers)]
         d = wl.to_device(case, dev)
         n = case.layers * copies[name]
-        kp = [d["k_pool"][l % case.layers].clone() if copies[name] > 1 else d["k_pool"][l]
-              for l in range(n)]
-        vp = [d["v_pool"][l % case.layers].clone() if copies[name] > 1 else d["v_pool"][l]
-              for l in range(n)]
-        del d["k_pool"], d["v_pool"]
+        if fp8:
+            del d["k_pool"], d["v_pool"]
+            kp = [k8[l % case.layers].to(dev) for l in range(n)]
+            vp = [v8[l % case.layers].to(dev) for l in range(n)]
+            del k8, v8
+        else:
+            kp = [d["k_pool"][l % case.layers].clone() if copies[name] > 1 else d["k_pool"][l]
+                  for l in range(n)]
+            vp = [d["v_pool"][l % case.layers].clone() if copies[name] > 1 else d["v_pool"][l]
+                  for l in range(n)]
+            del d["k_pool"], d["v_pool"]
         rows, hq, hk, hd = case.rows, case.q_heads, case.kv_heads, case.head_dim
         ws = ops.alloc_workspace(rows, hq, hk, hd, case.max_seq_len, case.block_size, device=dev)
         out = torch.zeros(n, rows, hq, hd, dtype=torch.float16, device=dev)
         has_append = bool((case.positions >= 0).any())
+        ks8 = torch.full((hk,), 0.12, dtype=torch.float32, device=dev)
+        vs8 = torch.full((hk,), 0.12, dtype=torch.float32, device=dev)
 
         def step():
             # positions < 0 (the shared-prefix rows) append nothing
             for l in range(n):
                 li = l % case.layers
-                ops.append_decode(out[l], d["q"][li], kp[l], vp[l], d["block_tables"],
-                                  d["seq_lens"], d["positions"], d["k_new"][li], d["v_new"][li],
-                                  case.scale, case.max_seq_len, ws, pdl=True)
+                if fp8:
+                    ops.append_decode_fp8(out[l], d["q"][li], kp[l], vp[l], ks8, vs8,
+                                          d["block_tables"], d["seq_lens"], d["positions"],
+                                          d["k_new"][li], d["v_new"][li], case.scale,
+                                          case.max_seq_len, ws, pdl=True)
+                else:
+                    ops.append_decode(out[l], d["q"][li], kp[l], vp[l], d["block_tables"],
+                                      d["seq_lens"], d["positions"], d["k_new"][li],
+                                      d["v_new"][li], case.scale, case.max_seq_len, ws, pdl=True)
 
         step()
         torch.cuda.synchronize()
@@ -341,6 +364,11 @@ def measure_configs(args, dev, peak, peak_kind):
         per_launch = ms * 1e-3 / n
         logical = b["decode_layer"] + b["append_layer"]
         unique = b["decode_layer_unique"] + b["append_layer"]
+        if fp8:
+            # one byte per cached element; the new token comes in as fp16 and goes out as codes
+            n_app = int((case.positions >= 0).sum())
+            logical = (b["kv_logical"] // 2 + b["q_out"] + b["table"]
+                       + n_app * hk * hd * (2 + 1) * 2)
         roof_bytes = unique if name == "shared" else logical
         achieved = roof_bytes / per_launch / 1e9
         entry = {
@@ -354,6 +382,7 @@ def measure_configs(args, dev, peak, peak_kind):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_kind},
             "what": ("append + decode (one fused launch)" if has_append else "decode")
+                    + (" over FP8 pools" if fp8 else "")
                     + (f", {copies[name]} pool copies" if copies[name] > 1 else ""),
         }
         if name == "shared":
@@ -362,6 +391,10 @@ def measure_configs(args, dev, peak, peak_kind):
             entry["GBps_logical"] = round(logical / per_launch / 1e9, 2)
         if name == "tiny":
             entry["note"] = "0.29 MB per launch: L2-resident; a launch-latency figure"
+        if fp8 and base in out_cfg:
+            # the same workload on fp16 pools: time and bandwidth ratios
+            entry["vs_fp16"] = {"time_ratio": round(out_cfg[base]["us_per_launch"] / entry["us_per_launch"], 3),
+                                "GBps_ratio": round(entry["GBps"] / out_cfg[base]["GBps"], 3)}
         out_cfg[name] = entry
         del g, kp, vp, d, out, ws
         torch.cuda.empty_cache()
