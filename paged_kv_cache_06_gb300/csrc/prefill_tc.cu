@@ -61,6 +61,27 @@
 
 namespace pkv {
 namespace prefill_tc {
+// Packed fp32 pairs (sm_100 family): two independent IEEE operations per
+// instruction, each rounded as its scalar form would be.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 
 using namespace ptx;
 
@@ -844,15 +865,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float mneg = m == -INFINITY ? 0.f : -m;
                 uint32_t pk[32];
-                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                // scores in pairs: one packed FMA for the exponents, one
+                // packed add for the row sums (two pairs of partial sums)
+                const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2), mn2 = f32x2(mneg, mneg);
+                uint64_t rs2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float e0 = fast_exp2(fmaf(s[2 * c], p.scale_log2, mneg));
-                    const float e1 = fast_exp2(fmaf(s[2 * c + 1], p.scale_log2, mneg));
+                    float x0, x1;
+                    f32x2_split(fma_f32x2(f32x2(s[2 * c], s[2 * c + 1]), sc2, mn2), x0, x1);
+                    const float e0 = fast_exp2(x0);
+                    const float e1 = fast_exp2(x1);
                     pk[c] = pack_half2(e0, e1);
-                    rs4[c & 3] += e0 + e1;
+                    rs2[c & 1] = add_f32x2(rs2[c & 1], f32x2(e0, e1));
                 }
-                l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+                float r0, r1, r2, r3;
+                f32x2_split(rs2[0], r0, r1);
+                f32x2_split(rs2[1], r2, r3);
+                l = l * alpha + ((r0 + r1) + (r2 + r3));
                 // O is rescaled only after the previous PV product is complete.
                 if (__any_sync(0xffffffffu, moved)) {
                     if (!(ok = mbar_waitw(bar_o + 8 * psb, psph, abort))) break;
