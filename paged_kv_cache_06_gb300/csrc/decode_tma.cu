@@ -285,12 +285,14 @@ __device__ __forceinline__ void softmax_step(Soft& st, float (&s)[4], int valid,
     // B fragments of P^T (token x head) by transposing in registers
     pb0 = movmatrix_t(px);
     pb1 = movmatrix_t(py);
+    // O rescaled by (al0, al1) per head pair, two lanes per packed multiply
+    const uint64_t al2 = f32x2(al0, al1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        st.o[i][0] *= al0;
-        st.o[i][1] *= al1;
-        st.o[i][2] *= al0;
-        st.o[i][3] *= al1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            f32x2_split(mul_f32x2(f32x2(st.o[i][2 * h], st.o[i][2 * h + 1]), al2), st.o[i][2 * h],
+                        st.o[i][2 * h + 1]);
     }
 }
 
