@@ -27,7 +27,7 @@
  *     o[r][h][:] = sum_t softmax(s)_t * V_t[:]
  * with kvh = h / (q_heads / kv_heads) (contiguous query-head groups).
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent:
  *   - seq_len == 0 gives an all-zero output row.
  *   - table entries past ceil(L/bs) are never read; an entry that is read and
  *     lies outside [0, num_blocks) is an error (return code ORACLE_BAD_TABLE).
