@@ -1,4 +1,4 @@
-// Paged decode attention for sm_103a: TMA-staged, tensor-core, stream-K.
+// Paged decode attention for sm_103a: asynchronously staged, tensor-core, stream-K.
 //
 // "PagedAttention" (deepconcepts.dev), sections "PagedAttention" and "What
 // the block table costs": the kernel walks each sequence's block table and
@@ -63,9 +63,9 @@
 // read.
 //
 // Safety: table entries are range-checked before any copy is issued (a bad
-// entry is skipped and flagged); every mbarrier wait and counter poll is
-// bounded and a timeout sets PKV_DEV_ERR_TIMEOUT, stops the block and drains
-// its copies in flight.
+// entry is skipped and flagged); every record poll is bounded, and a poll
+// that runs out sets PKV_DEV_ERR_TIMEOUT and stops the block (its copies have
+// all landed by then).
 #include <cuda.h>
 
 #include <mutex>
@@ -184,7 +184,6 @@ struct Smem {
 // dependent launch) at batch 32: 228 KB per SM, 1 KB reserved per block.
 static_assert(Smem::total(32) + 1024 <= 233472 / 2, "two blocks per SM at 32 rows");
 
-__device__ __forceinline__ const void* kmap_base(const Params& p, bool v) { return v ? p.vbase : p.kbase; }
 
 // ---------------------------------------------------------------------------
 // PTX wrappers (shared ones in ptx.cuh)
@@ -193,9 +192,6 @@ using namespace ptx;
 
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ int granules_of(int L) { return (L + kGranule - 1) / kGranule; }
@@ -1015,8 +1011,8 @@ __device__ void build_block_plan(BlockPlan* bp, const Params& p, bool paged, int
     __syncwarp();
 }
 
-// Per-row work of block cta, done by its producer warp after the dependency
-// wait (off the consumers' critical path): rows cta, cta + G, ... with nothing
+// Per-row work of block cta, done by its warp 7 after the dependency wait
+// (off the consumers' critical path): rows cta, cta + G, ... with nothing
 // to read get zero outputs, and in the fused form their new token is stored
 // into its slot (as E4M3 codes for FP8 pools, quantised exactly as
 // paged_kv_append_fp8 does).  The block that stages the slot's granule takes
@@ -1401,8 +1397,7 @@ __device__ void burst_emit(const PieceOut& po, const BlockPlan* bp, const unsign
 
 template <bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
-    decode_tma_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ Params prm) {
+    decode_tma_kernel(const __grid_constant__ Params prm) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1474,7 +1469,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     cx.Geff = Geff;
 
     if (warp == kConsumerWarps) {
-        // ============================ producer ============================
+        // ============================ row work ============================
         // Burst (or idle): the consumer warps stage their own granules; this
         // warp only does the block's row work after the dependency wait.
         griddep_wait();
@@ -1494,8 +1489,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             // This warp's granules go to their slots now, before the
             // dependency wait (the cached tokens are not written by the
             // preceding kernel; the appended one is patched in after it).
-            const unsigned char* kpool = reinterpret_cast<const unsigned char*>(kmap_base(p, false));
-            const unsigned char* vpool = reinterpret_cast<const unsigned char*>(kmap_base(p, true));
+            const unsigned char* kpool = reinterpret_cast<const unsigned char*>(p.kbase);
+            const unsigned char* vpool = reinterpret_cast<const unsigned char*>(p.vbase);
 #pragma unroll 1
             for (int g = bp->wa[warp]; g < bp->wb[warp]; ++g) {
                 const int si = g - g0, zrow = bp->szrow[si];
@@ -1638,18 +1633,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 
-// Tensor map over a pool viewed as [rows][hk][128] elements, 128-byte swizzle:
-// fp16, box 64 dims x 1 head x 16 tokens; FP8 (bytes), box 128 dims x 1 head
-// x 16 tokens.  Either way a box row is 128 bytes.
-static int pool_map(const void* base, int64_t rows, int hk, bool fp8, CUtensorMap* out) {
-    const int64_t esize = fp8 ? 1 : 2;
-    const int64_t dims[3] = {kHeadDim, hk, rows};
-    const int64_t strides[2] = {kHeadDim * esize, hk * kHeadDim * esize};
-    const int box[3] = {fp8 ? 128 : 64, 1, kGranule};
-    return tiled_map_3d(base, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        dims, strides, box, out);
-}
-
 // Test hooks for the bounded waits of the split-unit merge (see
 // pkv_debug_set_decode_hooks); zero / null in normal use.
 static std::mutex g_hook_mutex;
@@ -1780,9 +1763,6 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     int ctas = 0;
     if ((st = decode_grid(rows, kv_heads, limit, &ctas)) != PKV_OK) return st;
     if (plan && !paged) return PKV_ERR_UNSUPPORTED;
-    CUtensorMap km, vm;
-    if ((st = pool_map(k_base, pool_rows, kv_heads, fp8, &km)) != PKV_OK) return st;
-    if ((st = pool_map(v_base, pool_rows, kv_heads, fp8, &vm)) != PKV_OK) return st;
 
     Params prm{};
     prm.out = static_cast<__half*>(out);
@@ -1840,7 +1820,7 @@ int tma_decode_launch(void* out, const void* q, const void* k_base, const void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, kernel, km, vm, prm) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, prm) != cudaSuccess) return PKV_ERR_CUDA;
     return launch_status();
 }
 
