@@ -7,15 +7,18 @@
  *     cache is cut into fixed-size blocks; each sequence keeps a block table
  *     mapping its logical block n to the physical block holding it, and the
  *     attention kernel walks that table instead of striding a slab.
- *     Section "What the block table costs": the table is one dense int32
- *     array [max_num_reqs][max_num_blocks_per_req].
+ *     Section "What the block table costs": the tables of all rows form a
+ *     single dense int32 matrix, a row per request and a column per possible
+ *     logical block.
  *   - "Paged attention" (danielfleming.xyz), section "What changed": decode
- *     reads, per row, only the blocks its table lists, at the row's own
- *     length; a free list hands blocks out at admission (reserve on admit).
+ *     touches, for each row, just the blocks named in that row's table, up to
+ *     the row's true length; a request takes its blocks from a free list when
+ *     it is admitted (reserve on admit).
  *   - "SLM paged attention" (aicassindra.com), section "The architecture":
- *     one pre-allocated pool sliced into equal blocks; logical block =
- *     position / block_size; the last block fills slot by slot; shared
- *     prefix blocks carry a reference count and are copied on write.
+ *     the pool is allocated once and divided into fixed-size blocks; token
+ *     position p lives in logical block p / block_size; the final block fills
+ *     one slot at a time; blocks shared by a prefix are reference-counted and
+ *     copied before a write.
  *
  * Data layout (all device buffers, row-major, contiguous, 16-byte aligned):
  *   k_pool, v_pool   fp16 [num_blocks][block_size][kv_heads][head_dim]
@@ -106,8 +109,8 @@ int paged_kv_append(void* k_pool, void* v_pool, const int32_t* block_tables,
  * paged_kv_copy_blocks -- copy-on-write: for i < n, block dst_ids[i] of both
  * pools becomes a bit-exact copy of block src_ids[i].  Defining passage:
  * "SLM paged attention", sections "The architecture" and "End-to-end flow"
- * (a writer about to write into a shared block gets a clone of just that
- * block; its table entry is then repointed).  The pairs come from
+ * (a writer about to modify a block it shares receives a private copy of
+ * that block alone, and its table entry then points at the copy).  The pairs come from
  * pkv_bm_append_slot.  The dst ids must be distinct and must not appear among
  * the src ids of the same call (pairs run concurrently).  An id outside
  * [0, num_blocks) skips its pair and sets PKV_DEV_ERR_BLOCK_ID.
@@ -120,9 +123,9 @@ int paged_kv_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_ids,
 /*
  * paged_kv_prefill_scatter -- lay a batched prefill's K/V into the rows'
  * blocks with the padding dropped.  Defining passage: "Paged attention",
- * section "What changed" (newly admitted requests are prefilled together,
- * left padded to the group's widest prompt, after which each row's KV is
- * copied into its blocks with the padding dropped).
+ * section "What changed" (requests admitted together are prefilled as one
+ * batch, padded on the left to its longest prompt; each row's K/V then moves
+ * into the row's blocks without the padding).
  *
  * k_src, v_src: fp16 [rows][width][kv_heads][head_dim].  For each row r with
  * lengths[r] > 0, source columns src_start[r] .. src_start[r] + lengths[r] - 1
@@ -230,11 +233,11 @@ int paged_attention_append_decode(void* out, const void* q, void* k_pool, void* 
 
 /*
  * paged_attention_padded_decode -- the comparator the paged cache replaced:
- * attention over a contiguous slab with one full-width slot per row, computed
- * across the whole width for every row with columns past the row's length
- * masked out ("Continuous batching", danielfleming.xyz, sections "What
- * changed" and "Where the missing capacity went": the mask hides the data but
- * not the work).  Used to measure what reading true lengths saves.
+ * attention over a contiguous slab that gives every row a slot as wide as
+ * the widest row, computed across that whole width for every row with the
+ * columns past the row's length masked out ("Continuous batching",
+ * danielfleming.xyz, sections "What changed" and "Where the missing capacity
+ * went": masking removes the padded values from the result, not their cost).  Used to measure what reading true lengths saves.
  *
  * k_slab, v_slab: fp16 [rows][width][kv_heads][head_dim].  Row r's result
  * equals paged_attention_decode's on the same tokens; every column of the
@@ -250,8 +253,8 @@ int paged_attention_padded_decode(void* out, const void* q, const void* k_slab,
 /*
  * paged_attention_prefill -- chunked prefill: attention of several query
  * tokens per row, causal within the row's chunk.  Defining passages:
- * "Paged attention" (danielfleming.xyz), closing sections (long prompts split
- * into fixed chunks, 512 tokens, so decode steps interleave) and
+ * "Paged attention" (danielfleming.xyz), closing sections (long prompts
+ * broken into fixed-size pieces of 512 tokens, with decode steps in between) and
  * "PagedAttention" (deepconcepts.dev), section "PagedAttention" (keys gathered
  * through the row's block table).
  *

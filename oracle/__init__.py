@@ -15,10 +15,11 @@ Citations (page title, section):
   * "PagedAttention" (deepconcepts.dev), "PagedAttention" and the closing note
     on FlashAttention: paged attention computes exactly ordinary attention;
     block-wise softmax recombination is exact.
-  * "Paged attention" (danielfleming.xyz), "What changed": decode reads only
-    the listed blocks at the row's true length.
-  * "SLM paged attention" (aicassindra.com), "The architecture": table maps
-    position / block_size to a physical block; last block partially filled.
+  * "Paged attention" (danielfleming.xyz), "What changed": decode touches
+    just the blocks a row's table names, up to its true length.
+  * "SLM paged attention" (aicassindra.com), "The architecture": a row's
+    table turns position / block_size into a physical block; the final block
+    may be partly filled.
 
 Parity pins: every function here is pinned by tests in ``tests/test_oracle.py``
 (brute force, closed forms, invariants); none is "parity unpinned".

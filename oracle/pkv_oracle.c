@@ -14,11 +14,12 @@
  *     exact attention; splitting the softmax sum over blocks and recombining
  *     it does not change the result).
  *   - "Paged attention" (danielfleming.xyz), section "What changed": decode
- *     reads, for every row, only the blocks its table lists, at the row's own
- *     length.
+ *     touches, for each row, just the blocks named in the row's table, up to
+ *     the row's true length.
  *   - "SLM paged attention" (aicassindra.com), section "The architecture":
- *     the table maps position / block_size to a physical block id, and the
- *     last block is filled up to a count of slots.
+ *     a row's table turns a logical block index (position / block_size) into
+ *     a physical block id, and a slot count says how far the final block is
+ *     filled.
  *
  * So the oracle is the plain definition of attention over a row's tokens in
  * logical order, in double precision:
@@ -180,8 +181,8 @@ int oracle_paged_decode(double* out, const uint16_t* q, const uint16_t* k_pool,
 
 /*
  * Contiguous decode over a padded slab, the layout the paged cache replaced
- * ("Continuous batching", section "What changed": one full-width slot per
- * row).  k_slab, v_slab: [rows][width][kv_heads][head_dim]; row r uses its
+ * ("Continuous batching", section "What changed": every row owns a slot as
+ * wide as the widest row).  k_slab, v_slab: [rows][width][kv_heads][head_dim]; row r uses its
  * first seq_lens[r] tokens.
  */
 int oracle_contiguous_decode(double* out, const uint16_t* q, const uint16_t* k_slab,
@@ -314,9 +315,9 @@ int oracle_blockwise_decode(double* out, double* lse_out, const uint16_t* q,
 /*
  * Append: for each row r with positions[r] >= 0, the new token's K and V go
  * to slot (pos % bs) of physical block table[r][pos / bs], for every KV head
- * ("SLM paged attention", section "The architecture": the table maps
- * position / block_size to a physical block and the last block is filled one
- * slot at a time).  Operates in place on k_pool / v_pool, as a plain copy of
+ * ("SLM paged attention", section "The architecture": a row's table
+ * turns position / block_size into a physical block, and the final block
+ * takes one slot after another).  Operates in place on k_pool / v_pool, as a plain copy of
  * the fp16 bit patterns.  Rows with a negative position are skipped.
  */
 int oracle_paged_append(uint16_t* k_pool, uint16_t* v_pool, const int32_t* block_tables,
@@ -349,8 +350,8 @@ int oracle_paged_append(uint16_t* k_pool, uint16_t* v_pool, const int32_t* block
 /*
  * Copy-on-write block copy: for i < n, block dst_ids[i] of both pools becomes
  * a byte copy of block src_ids[i] ("SLM paged attention", section "The
- * architecture": the manager clones just the shared block a writer must
- * write into and repoints the writer's table entry).  In place; pairs are
+ * architecture": a writer about to modify a shared block gets a private
+ * copy of that one block, and its table entry is switched to the copy).  In place; pairs are
  * applied in order.  Ids outside [0, num_blocks) are an error.
  */
 int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* src_ids,
@@ -371,9 +372,9 @@ int oracle_copy_blocks(uint16_t* k_pool, uint16_t* v_pool, const int32_t* src_id
 }
 
 /*
- * Prefill scatter: after a batched prefill whose rows were left-padded to the
- * group's widest prompt, each row's K/V is copied into its blocks with the
- * padding dropped ("Paged attention", section "What changed").  Source
+ * Prefill scatter: a batched prefill pads its rows on the left to the longest
+ * prompt of the batch; afterwards each row's K/V moves into the row's blocks
+ * without the padding ("Paged attention", section "What changed").  Source
  * k_src, v_src: [rows][width][kv_heads][head_dim]; row r's tokens are columns
  * src_start[r] .. src_start[r] + lengths[r] - 1 and go to logical positions
  * dst_start[r] .. dst_start[r] + lengths[r] - 1 of the row's table.  Rows
@@ -580,9 +581,10 @@ int oracle_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_poo
 /*
  * Chunked prefill: several query tokens per row, causal within the chunk.
  * "Paged attention" (danielfleming.xyz), section "What changed" and the
- * closing paragraphs: the next engine splits long prompts into fixed chunks
- * (512 tokens) so decode steps run between them; "Continuous batching", the
- * closing section: split a long prefill into fixed size chunks.  Reading
+ * closing paragraphs: the following engine breaks long prompts into pieces of
+ * a fixed size (512 tokens) and runs decode steps in between; "Continuous
+ * batching", closing section: chunking long prefills is named as the next
+ * step.  Reading
  * taken (the pages give no kernel): row r's chunk holds the
  * C_r = q_start[r+1] - q_start[r] newest tokens of the row, at positions
  * p_r + i with p_r = seq_lens[r] - C_r (their K/V already in the row's

@@ -1,8 +1,8 @@
 // paged_kv_append: write each row's new K/V token into its slot.
 //
-// "SLM paged attention" (aicassindra.com), section "The architecture": the
-// block table maps logical block index (position / block_size) to a physical
-// block id and the last block fills one slot at a time.
+// "SLM paged attention" (aicassindra.com), section "The architecture": a
+// row's table turns the logical block index (position / block_size) into a
+// physical block id, and the final block takes one slot after another.
 //
 // One thread block per row; each thread moves 16-byte vectors.  Per layer at
 // 32 rows this is 32 KB of traffic, so the kernel is launch-latency bound.

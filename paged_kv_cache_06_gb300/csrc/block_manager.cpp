@@ -1,8 +1,8 @@
 // Host-side block manager for the paged KV pool.
 //
-// "Paged attention" (danielfleming.xyz), section "What changed": blocks come
-// from a free list at admission and go back when a request finishes, with no
-// copy; reserve on admit takes every block the request could ever need
+// "Paged attention" (danielfleming.xyz), section "What changed": a request
+// takes its blocks off a free list when it is admitted and returns them when
+// it finishes, and nothing is copied; reserve on admit takes every block the request could ever need
 // (prompt + full token budget) or admits nothing.
 // "SLM paged attention" (aicassindra.com), sections "The architecture" and
 // "End-to-end flow": O(1) pop/push free list; without a reservation a

@@ -1,11 +1,11 @@
 // Block copies for copy-on-write, and the prefill scatter into blocks.
 //
 // "SLM paged attention" (aicassindra.com), sections "The architecture" and
-// "End-to-end flow": when a sequence must write into a block it shares, the
-// manager clones just that block and repoints the writer's table entry.
-// "Paged attention" (danielfleming.xyz), section "What changed": after a
-// batched prefill, left-padded to the group's widest prompt, each row's KV is
-// copied into its blocks with the padding dropped.
+// "End-to-end flow": a sequence about to write into a block it shares gets a
+// private copy of that one block, and its table entry is switched to the
+// copy.  "Paged attention" (danielfleming.xyz), section "What changed": a
+// batched prefill pads its rows on the left to the batch's longest prompt,
+// and each row's K/V then moves into the row's blocks without the padding.
 //
 // Both are pure data movement: 16-byte vectors, consecutive threads on
 // consecutive addresses, grids sized in whole blocks of work.

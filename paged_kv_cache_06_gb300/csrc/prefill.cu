@@ -2,10 +2,10 @@
 // The kernel (tcgen05 tensor cores, accumulators in tensor memory) is in
 // prefill_tc.cu.
 //
-// "Paged attention" (danielfleming.xyz), closing sections: the next engine
-// splits long prompts into fixed chunks (512 tokens) so decode steps run
-// between them; "Continuous batching", closing section: a long prefill split
-// into fixed size chunks.  Row r's chunk is its newest
+// "Paged attention" (danielfleming.xyz), closing sections: the following
+// engine breaks long prompts into pieces of a fixed size (512 tokens) and runs
+// decode steps in between; "Continuous batching", closing section: chunking
+// long prefills is named as the next step.  Row r's chunk is its newest
 // C_r = q_start[r+1] - q_start[r] tokens, already written to the row's blocks;
 // query i sits at position p_r + i (p_r = seq_lens[r] - C_r) and attends to
 // the row's tokens 0 .. p_r + i.

@@ -2,8 +2,8 @@
 // (tcgen05, accumulators and the probabilities in tensor memory), sm_103a.
 //
 // What it computes is paged_attention_prefill's definition ("Paged
-// attention", danielfleming.xyz, closing sections: long prompts split into
-// fixed chunks so decode steps interleave; "PagedAttention", deepconcepts.dev,
+// attention", danielfleming.xyz, closing sections: long prompts broken
+// into fixed-size pieces with decode steps in between; "PagedAttention", deepconcepts.dev,
 // section "PagedAttention": keys gathered through the row's block table):
 // query i of row r's chunk sits at position seq_lens[r] - C_r + i and attends
 // causally to the row's tokens 0 .. that position.

@@ -3,7 +3,7 @@
 Append and block-table indexing must be bit-exact; attention outputs must
 satisfy |gpu - oracle| <= 2e-3 + 2e-3 * |oracle| elementwise (fp16 output of
 fp32 arithmetic; the pages report the paged kernel's fp16 outputs differing
-from the contiguous kernel's by about one part in a thousand).
+from the contiguous kernel's by roughly 1e-3 relative).
 """
 import numpy as np
 import pytest
