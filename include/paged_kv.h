@@ -482,7 +482,11 @@ int pkv_debug_set_decode_hooks(unsigned poll_limit, const void* stuck_word);
 /*
  * pkv_check_error -- synchronise `stream`, copy the device error word to
  * *host_err and clear it on the device.  Returns PKV_ERR_CUDA if the stream
- * reported an error.  The only library call that blocks.
+ * reported an error.  The only library call that blocks.  If the word holds
+ * PKV_DEV_ERR_TIMEOUT, the outputs of the calls that reported into it are
+ * invalid, and every decode or prefill workspace those calls used must be
+ * zero-filled again before its next use (the library's own scratch is
+ * cleared by its next call).
  */
 int pkv_check_error(int32_t* dev_err, cudaStream_t stream, int32_t* host_err);
 
