@@ -386,18 +386,10 @@ __device__ __forceinline__ void attend8(Soft& st, const uint32_t (&qb)[16], cons
     }
 }
 
-// Query fragments of heads kvh*group .. +7 of row r: b0 = Q[head gq][16ks + 2tq..],
-// b1 = Q[head gq][16ks + 8 + 2tq..] (heads past the group are zero).
-__device__ __forceinline__ void load_q(uint32_t (&qb)[16], const uint32_t* qrow, bool live, int tq) {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        qb[2 * ks] = live ? qrow[ks * 8 + tq] : 0u;
-        qb[2 * ks + 1] = live ? qrow[ks * 8 + 4 + tq] : 0u;
-    }
-}
-// The same from global memory, for a group's first head row `q0`: heads past
-// the group repeat its last head (every head is its own MMA column, so those
-// columns are computed and never stored).
+// Query fragments of the heads of a group, from global memory, for the
+// group's first head row `q0`: b0 = Q[head gq][16ks + 2tq..], b1 = Q[head
+// gq][16ks + 8 + 2tq..]; heads past the group repeat its last head (every head
+// is its own MMA column, so those columns are computed and never stored).
 __device__ __forceinline__ void load_q_global(uint32_t (&qb)[16], const __half* q0, int group, int lane) {
     const int h = (lane >> 2) < group ? (lane >> 2) : group - 1;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q0 + h * kHeadDim) + (lane & 3);
@@ -421,32 +413,6 @@ __device__ __forceinline__ void load_q_fp8(uint32_t (&qb)[16], const __half* q0,
         qb[4 * i + 2] = v.z;
         qb[4 * i + 3] = v.w;
     }
-}
-
-// Prepares a staged granule for attend: zeroes V rows past `valid` (they may
-// hold anything, NaN included) and overwrites row patch_row with the new
-// token (lanes 0-15 carry its K, lanes 16-31 its V, 16 bytes each).  Returns
-// whether shared memory was written.
-__device__ __forceinline__ bool prepare_granule(unsigned char* slot_ptr, int valid, int patch_row,
-                                                const uint4& patch_val, int lane) {
-    bool wrote = false;
-    if (valid < kGranule) {
-        uint4* v0 = reinterpret_cast<uint4*>(slot_ptr + kSlotV);
-        for (int i = lane; i < (kGranule - valid) * 8; i += 32) {
-            const int row = valid + (i >> 3);
-            v0[row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
-            v0[kBoxBytes / 16 + row * 8 + (i & 7)] = make_uint4(0, 0, 0, 0);
-        }
-        wrote = true;
-    }
-    if (patch_row >= 0 && patch_row < valid) {
-        const int c16 = lane & 15;  // 16-byte chunk of the 128 dims
-        unsigned char* box = slot_ptr + (lane < 16 ? 0u : kSlotV) + (c16 >> 3) * kBoxBytes;
-        *reinterpret_cast<uint4*>(box + patch_row * 128 + (((c16 & 7) ^ (patch_row & 7)) << 4)) =
-            patch_val;
-        wrote = true;
-    }
-    return wrote;
 }
 
 // The copies of stage_granule, from the byte offset `row0` of the granule's
@@ -1542,7 +1508,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             const float sl2 = kFp8 ? p.scale_log2 * sm_ks[kvh] : p.scale_log2;
-            const bool ok = true;
             // this lane's copies have landed; then every lane's
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             __syncwarp();
@@ -1565,7 +1530,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // the chunks of all of them.
             const int k = bp->pwn[pi];
             if (k > 1) {
-                if (ok) dump_state(st, smem + Smem::ring + (a - g0) * kSlotBytes, lane);
+                dump_state(st, smem + Smem::ring + (a - g0) * kSlotBytes, lane);
                 named_sync(kBarPiece + pi, k * 32);
             }
             if (!sm_flags[0]) {
